@@ -1,0 +1,151 @@
+"""Seeded synthetic inputs shared by the oracle side and the CUDA side.
+
+This module holds no attention arithmetic: it only draws numbers.  Both the
+tests (oracle side) and the CUDA binding side get their Q, K, V, dO from here,
+so that the two are fed the same rounded values.
+
+Generator (counter-based, every element independent of how many others are
+drawn, so a single head can be regenerated alone):
+
+* SplitMix64 (G. Steele, D. Lea, C. Flood, "Fast splittable pseudorandom number
+  generators", OOPSLA 2014): output_n = mix(key + (n + 1) * 0x9E3779B97F4A7C15)
+  with the published 64-bit finaliser ``mix``.
+* Two outputs per pair -> two doubles in (0, 1] from their top 53 bits ->
+  Box-Muller (G. Box, M. Muller 1958): r = sqrt(-2 ln u1), angles 2 pi u2.
+* float32 sample * sigma, then round-to-nearest-even to bfloat16 or float16.
+
+The per-head key is mix(base_seed ^ mix(tensor_id * 2^32 + head)), so head h of
+tensor t is the same whichever subset of heads is drawn.
+"""
+from __future__ import annotations
+
+from concurrent.futures import ThreadPoolExecutor
+import os
+
+import numpy as np
+
+GAMMA = np.uint64(0x9E3779B97F4A7C15)
+_M1 = np.uint64(0xBF58476D1CE4E5B9)
+_M2 = np.uint64(0x94D049BB133111EB)
+
+TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "do": 4}
+
+
+def _mix(z: np.ndarray) -> np.ndarray:
+    """SplitMix64 finaliser on a uint64 array (wrapping arithmetic)."""
+    z = (z ^ (z >> np.uint64(30))) * _M1
+    z = (z ^ (z >> np.uint64(27))) * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def _mix_scalar(x: int) -> int:
+    with np.errstate(over="ignore"):
+        return int(_mix(np.array([x & 0xFFFFFFFFFFFFFFFF], dtype=np.uint64))[0])
+
+
+def head_key(base_seed: int, tensor_id: int, head: int) -> int:
+    inner = _mix_scalar((tensor_id << 32) + head)
+    return _mix_scalar((base_seed & 0xFFFFFFFFFFFFFFFF) ^ inner)
+
+
+def splitmix64_stream(key: int, n: int) -> np.ndarray:
+    """First n outputs of the SplitMix64 stream with the given key."""
+    with np.errstate(over="ignore"):
+        ctr = np.arange(1, n + 1, dtype=np.uint64)
+        return _mix(np.uint64(key) + ctr * GAMMA)
+
+
+def standard_normal(key: int, n: int) -> np.ndarray:
+    """n float32 standard-normal samples from one SplitMix64 stream."""
+    m = (n + 1) // 2
+    bits = splitmix64_stream(key, 2 * m)
+    # top 53 bits -> (0, 1]: (k + 1) / 2^53
+    u = ((bits >> np.uint64(11)).astype(np.float64) + 1.0) * (1.0 / 9007199254740992.0)
+    u1, u2 = u[0::2], u[1::2]
+    r = np.sqrt(-2.0 * np.log(u1))
+    t = 2.0 * np.pi * u2
+    out = np.empty(2 * m, dtype=np.float64)
+    out[0::2] = r * np.cos(t)
+    out[1::2] = r * np.sin(t)
+    return out[:n].astype(np.float32)
+
+
+def round_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    r = (u + np.uint64(0x7FFF) + ((u >> np.uint64(16)) & np.uint64(1))) >> np.uint64(16)
+    return r.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def round_fp16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> float16 bit patterns (numpy's cast rounds to nearest even)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def fp16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return np.asarray(b, dtype=np.uint16).view(np.float16).astype(np.float32)
+
+
+def to_bits(x: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return round_bf16_bits(x)
+    if dtype == "fp16":
+        return round_fp16_bits(x)
+    raise ValueError(dtype)
+
+
+def bits_to_f32(b: np.ndarray, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return bf16_bits_to_f32(b)
+    if dtype == "fp16":
+        return fp16_bits_to_f32(b)
+    raise ValueError(dtype)
+
+
+def tensor_heads(base_seed: int, name: str, BH: int, N: int, d: int, sigma: float,
+                 dtype: str = "bf16", heads=None, threads: int | None = None) -> np.ndarray:
+    """16-bit patterns [len(heads), N, d] of tensor `name` for the given heads
+    (default: all BH heads), entries ~ N(0, sigma^2) rounded to `dtype`."""
+    if heads is None:
+        heads = range(BH)
+    heads = list(heads)
+    tid = TENSOR_IDS[name]
+    out = np.empty((len(heads), N, d), dtype=np.uint16)
+
+    def one(ix):
+        h = heads[ix]
+        z = standard_normal(head_key(base_seed, tid, h), N * d) * np.float32(sigma)
+        out[ix] = to_bits(z, dtype).reshape(N, d)
+
+    nthr = threads or min(len(heads), os.cpu_count() or 1, 16)
+    if nthr <= 1 or len(heads) <= 1:
+        for ix in range(len(heads)):
+            one(ix)
+    else:
+        with ThreadPoolExecutor(nthr) as ex:
+            list(ex.map(one, range(len(heads))))
+    return out
+
+
+def late_spike(q_bits: np.ndarray, k_bits: np.ndarray, dtype: str, alpha: float,
+               rows, tile: int = 128) -> np.ndarray:
+    """Adversarial 'late spike' keys for one head (q_bits, k_bits: [N, d]).
+
+    For each query row i in `rows`, key (last tile start + i mod tile) is set to
+    alpha * q_i / |q_i|, so that row's largest score arrives in the final key
+    tile.  Returns new key bits [N, d]."""
+    q = bits_to_f32(q_bits, dtype).astype(np.float64)
+    k = bits_to_f32(k_bits, dtype).astype(np.float32).copy()
+    N = q.shape[0]
+    last = ((N - 1) // tile) * tile
+    for i in rows:
+        j = last + (i % tile)
+        if j >= N:
+            j = N - 1
+        nrm = np.linalg.norm(q[i]) or 1.0
+        k[j] = (alpha * q[i] / nrm).astype(np.float32)
+    return to_bits(k, dtype)
