@@ -1,0 +1,163 @@
+"""Python binding of libattn_gb300.so (the C ABI declared in include/attn.h).
+
+Argument marshalling only: every step of the forward and backward pass runs in
+the library's CUDA kernels.  PyTorch supplies device memory and streams.  If the
+library is missing or fails to load, every call raises; there is no fallback.
+
+Names mirror the C ABI:
+    attn_fwd(q, k, v, o, lse, scale, causal, stream=None)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream=None)
+    attn_bwd_workspace_size(B, H, N, d)
+    attn_last_device_error(stream=None)
+plus two allocating conveniences, ``forward`` and ``backward``.
+Tensors are contiguous CUDA tensors [B, H, N, d] of bfloat16 or float16; lse
+is float32 [B, H, N].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_last_device_error",
+    "attn_status_string", "attn_last_launch_count", "forward", "backward", "library_path", "load",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libattn_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+ATTN_OK = 0
+ATTN_BF16, ATTN_FP16 = 0, 1
+
+EXPORTS = (
+    "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex",
+    "attn_status_string", "attn_last_device_error", "attn_last_launch_count",
+)
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {attn_status_string(status)} (status {status})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load the library (build it first with ``build.build()``); raises if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"{_LIB_PATH} is missing: build it with `python -m exact_attention_flashattention_gb300.build` "
+                "(nvcc, sm_103a).  There is no fallback implementation.")
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, vp]
+        lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
+        lib.attn_bwd.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, vp]
+        lib.attn_bwd_ex.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, vp]
+        lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
+        lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_status_string.argtypes = [i]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_last_device_error.argtypes = [vp]
+        lib.attn_last_launch_count.argtypes = []
+        for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_last_device_error,
+                   lib.attn_last_launch_count):
+            fn.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def attn_status_string(status: int) -> str:
+    return load().attn_status_string(int(status)).decode()
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(int(stream.cuda_stream))
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_BF16
+    if t.dtype == torch.float16:
+        return ATTN_FP16
+    raise TypeError(f"unsupported dtype {t.dtype}: bfloat16 or float16")
+
+
+def _check(t, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_fwd(q, k, v, o, lse, scale: float, causal: bool, stream=None) -> None:
+    """Queue the forward pass.  q, k, v, o: [B, H, N, d]; lse: float32 [B, H, N]."""
+    lib = load()
+    B, H, N, d = q.shape
+    st = lib.attn_fwd_ex(_check(q, "q"), _check(k, "k"), _check(v, "v"), _check(o, "o"), _check(lse, "lse"),
+                         B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd")
+
+
+def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
+    return int(load().attn_bwd_workspace_size(B, H, N, d))
+
+
+def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, stream=None) -> None:
+    """Queue the backward pass.  workspace: a CUDA uint8 tensor of at least
+    attn_bwd_workspace_size(B, H, N, d) bytes."""
+    lib = load()
+    B, H, N, d = q.shape
+    st = lib.attn_bwd_ex(_check(q, "q"), _check(k, "k"), _check(v, "v"), _check(o, "o"), _check(dout, "dout"),
+                         _check(lse, "lse"), _check(dq, "dq"), _check(dk, "dk"), _check(dv, "dv"),
+                         _check(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                         B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd")
+
+
+def attn_last_device_error(stream=None) -> int:
+    return int(load().attn_last_device_error(_stream_handle(stream)))
+
+
+def attn_last_launch_count() -> int:
+    return int(load().attn_last_launch_count())
+
+
+def forward(q, k, v, scale=None, causal=False, stream=None):
+    """Allocate O and L, queue the forward pass, return (O, L)."""
+    import torch
+    d = q.shape[-1]
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    return o, lse
+
+
+def backward(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None, stream=None):
+    """Allocate dQ, dK, dV (and the workspace if not given), queue the backward pass."""
+    import torch
+    B, H, N, d = q.shape
+    scale = d ** -0.5 if scale is None else scale
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        workspace = torch.empty(attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
+    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+    return dq, dk, dv

@@ -1,0 +1,228 @@
+// C-ABI entry points of libattn_gb300.so: argument checks, tensor-map
+// encoding, workspace carving and kernel dispatch.  Declared in include/attn.h.
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "attn_internal.h"
+
+namespace gb300 {
+
+// Device error word written by kernels whose bounded waits gave up.
+__device__ int g_device_error = 0;
+
+namespace {
+
+thread_local int t_last_launches = 0;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+struct DevInfo {
+    int sms = 0;
+    int* err_ptr = nullptr;
+};
+
+// Per-device cache of the SM count and of the device address of the error word.
+bool dev_info(DevInfo& out) {
+    static std::mutex mu;
+    static DevInfo cache[64];
+    static bool have[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!have[dev]) {
+        DevInfo di;
+        if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err_ptr), g_device_error) != cudaSuccess) return false;
+        cache[dev] = di;
+        have[dev] = true;
+    }
+    out = cache[dev];
+    return true;
+}
+
+// [BH, N, d] 16-bit tensor, box {64, 128, 1}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status_t check_sizes(int B, int H, int N, int d) {
+    if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (N % 128 != 0) return ATTN_ERR_UNSUPPORTED;
+    const long long total = (long long)B * H * N * d;
+    if (total >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t delta, lse2, dq_acc, total;
+};
+WsLayout ws_layout(int B, int H, int N, int d) {
+    WsLayout w;
+    const size_t rows = (size_t)B * H * N;
+    w.delta = 0;
+    w.lse2 = align_up(w.delta + rows * 4, 256);
+    w.dq_acc = align_up(w.lse2 + rows * 4, 256);
+    w.total = align_up(w.dq_acc + rows * (size_t)d * 4, 256);
+    return w;
+}
+
+}  // namespace
+}  // namespace gb300
+
+using namespace gb300;
+
+extern "C" {
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+    t_last_launches = 0;
+    if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_sizes(B, H, N, d);
+    if (st != ATTN_OK) return st;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_ALIGNMENT;
+    DevInfo di;
+    if (!dev_info(di)) return ATTN_ERR_CUDA;
+    FwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int BH = B * H;
+    if (!make_map(&a.tm_q, q, BH, N, d) || !make_map(&a.tm_k, k, BH, N, d) || !make_map(&a.tm_v, v, BH, N, d))
+        return ATTN_ERR_CUDA;
+    a.o = o;
+    a.lse = lse;
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.fp16 = dtype == ATTN_FP16;
+    a.num_sms = di.sms;
+    a.error = di.err_ptr;
+    if (launch_fwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_launches = 1;
+    return ATTN_OK;
+}
+
+attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+                       float scale, int causal, void* stream) {
+    return attn_fwd_ex(q, k, v, o, lse, B, H, N, d, scale, causal, ATTN_BF16, stream);
+}
+
+size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
+    if (check_sizes(B, H, N, d) != ATTN_OK) return 0;
+    return ws_layout(B, H, N, d).total;
+}
+
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+    t_last_launches = 0;
+    if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_sizes(B, H, N, d);
+    if (st != ATTN_OK) return st;
+    const WsLayout w = ws_layout(B, H, N, d);
+    if (!workspace || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGNMENT;
+    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return ATTN_ERR_ALIGNMENT;
+    DevInfo di;
+    if (!dev_info(di)) return ATTN_ERR_CUDA;
+    BwdArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int BH = B * H;
+    if (!make_map(&a.tm_q, q, BH, N, d) || !make_map(&a.tm_k, k, BH, N, d) || !make_map(&a.tm_v, v, BH, N, d) ||
+        !make_map(&a.tm_do, dout, BH, N, d))
+        return ATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.delta = reinterpret_cast<float*>(ws + w.delta);
+    a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
+    a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+    a.BH = BH;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.fp16 = dtype == ATTN_FP16;
+    a.num_sms = di.sms;
+    a.error = di.err_ptr;
+    if (launch_bwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_launches = 3;
+    return ATTN_OK;
+}
+
+attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                       const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B,
+                       int H, int N, int d, float scale, int causal, void* stream) {
+    return attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                       ATTN_BF16, stream);
+}
+
+const char* attn_status_string(attn_status_t s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: null pointer, non-positive size or bad dtype";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: d must be 64 or 128, N a multiple of 128";
+        case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT: pointers must be 16-byte aligned (workspace 256)";
+        case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT: a kernel wait gave up; outputs are incomplete";
+    }
+    return "unknown attn_status_t";
+}
+
+attn_status_t attn_last_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+        return ATTN_ERR_TIMEOUT;
+    }
+    return ATTN_OK;
+}
+
+int attn_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

@@ -1,0 +1,462 @@
+// Fused attention backward for sm_103a: preprocess, main tcgen05 kernel and
+// dQ conversion ("Writing Speed-of-Light Attention Backward Kernel for 5090
+// in CUDA", sections "Mathematical Formulation" and the tiled pseudocode that
+// follows it: one CTA owns dK_j and dV_j of a key/value tile j, loops over the
+// query tiles i it interacts with, and adds each dQ_i partial into an FP32
+// accumulator; a second kernel converts that accumulator after a kernel
+// boundary).
+//
+// sm_103a mapping (transposed formulation, keys on TMEM lanes):
+//   S^T  = K_j Q_i^T      SS-MMA  -> TMEM [256,384)   (P^T written over it)
+//   dP^T = V_j dO_i^T     SS-MMA  -> TMEM [384,512)   (dS^T written over it)
+//   dV  += P^T dO_i       TS-MMA  (A = P^T from TMEM) -> TMEM [0,128)
+//   dK  += dS^T Q_i       TS-MMA  (A = dS^T from TMEM) -> TMEM [128,256)
+//   dQ_i = dS K_j         SS-MMA  (A = dS from shared memory) -> TMEM [256,384)
+// The transposes follow from the equations: dV = P^T dO and dK = dS^T Q need
+// P^T and dS^T as the left operand, which the tensor core can read straight
+// from TMEM when the scores are computed with keys on the lanes.
+//
+// CTA layout (512 threads): warps 0-7 elementwise (P, dS; warp w handles TMEM
+// lane quadrant w%4 and query columns [64 (w/4), +64)), warps 8-11 dQ drain
+// and dK/dV epilogue, warp 12 MMA issuer (owns TMEM), warp 13 TMA producer.
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kPanelBytes = 128 * 128;
+
+// ---------------------------------------------------------------- preprocess
+// D_r = sum_c dO[r,c] O[r,c] (FP32), lse2_r = L_r log2(e), dq_acc[r,:] = 0.
+// A group of D/8 threads handles one row; each thread reads 16 bytes of O and dO.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
+                                                      const float* __restrict__ lse, float* __restrict__ delta,
+                                                      float* __restrict__ lse2, float4* __restrict__ dq_acc,
+                                                      long rows) {
+    constexpr int TPR = D / 8;
+    const long total = rows * TPR;
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const uint4 a = __ldg(o + i);
+        const uint4 b = __ldg(dout + i);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+        float acc = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            float2 fa, fb;
+            if constexpr (BF16) {
+                fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+                fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+            } else {
+                fa = __half22float2(*reinterpret_cast<const __half2*>(&av[e]));
+                fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
+            }
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+        const unsigned mask = __activemask();
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
+        const long row = i / TPR;
+        const int part = (int)(i % TPR);
+        dq_acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (part == 0) {
+            delta[row] = acc;
+            lse2[row] = lse[row] * kLog2e;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- dQ convert
+template <bool BF16>
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
+                                                         long n8) {
+    const long stride = (long)gridDim.x * blockDim.x;
+    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
+        const float4 a = acc[2 * i], b = acc[2 * i + 1];
+        dq[i] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+    }
+}
+
+// ---------------------------------------------------------------- main kernel
+template <int D>
+struct BwdLayout {
+    static constexpr int kTile = 128 * D * 2;
+    static constexpr int kPanels = D / 64;
+    static constexpr int kK = 0;
+    static constexpr int kV = kTile;
+    static constexpr int kQ = 2 * kTile;          // [2 stages]
+    static constexpr int kDO = 4 * kTile;         // [2 stages]
+    static constexpr int kDS = 6 * kTile;         // dS^T, 128 x 128 16-bit, 2 panels
+    static constexpr int kAux = kDS + 2 * kPanelBytes;
+    static constexpr int kBarKVFull = 0, kBarKVEmpty = 1;
+    static constexpr int kBarQFull = 2;    // [2]
+    static constexpr int kBarQEmpty = 4;   // [2]
+    static constexpr int kBarSdpFull = 6, kBarDsReady = 7, kBarDsFree = 8;
+    static constexpr int kBarDqFull = 9, kBarDqFree = 10, kBarDkvFull = 11, kBarDkvEmpty = 12;
+    static constexpr int kBarTeardown = 13;
+    static constexpr int kNumBars = 14;
+    static constexpr int kMiscOff = kAux + kNumBars * 8;
+    static constexpr int kBytes = kMiscOff + 16;
+    static constexpr int kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384, kTmemDQ = 256;
+};
+
+struct BwdItem {
+    int bh, j, i0, n;   // head, key/value tile, first query tile, number of query tiles
+};
+__device__ __forceinline__ BwdItem decode_bwd(int idx, int T, int causal) {
+    BwdItem w;
+    w.bh = idx / T;
+    w.j = idx % T;     // within a head, j = 0 (the longest under the causal mask) first
+    w.i0 = causal ? w.j : 0;
+    w.n = T - w.i0;
+    return w;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
+                void* __restrict__ dk_out, void* __restrict__ dv_out, int BH, int N, float scale, int causal,
+                int* error) {
+    using L = BwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kAux);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int T = N / 128;
+    const int n_items = BH * T;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::kBarKVFull], 1);
+        mbar_init(&bars[L::kBarKVEmpty], 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars[L::kBarQFull + s], 1);
+            mbar_init(&bars[L::kBarQEmpty + s], 1);
+        }
+        mbar_init(&bars[L::kBarSdpFull], 1);
+        mbar_init(&bars[L::kBarDsReady], 256);
+        mbar_init(&bars[L::kBarDsFree], 1);
+        mbar_init(&bars[L::kBarDqFull], 1);
+        mbar_init(&bars[L::kBarDqFree], 128);
+        mbar_init(&bars[L::kBarDkvFull], 1);
+        mbar_init(&bars[L::kBarDkvEmpty], 128);
+        mbar_init(&bars[L::kBarTeardown], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 12) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (warp == 13 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+        prefetch_tensormap(&tm_do);
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitGuard guard{abort_flag, error, kWaitLimitNs};
+    const float scale_log2 = scale * kLog2e;
+
+    if (warp < 8) {
+        regs_inc<144>();
+        // ------------------------------------------------------ P and dS (elementwise)
+        const int half = warp >> 2;
+        const int row = (warp & 3) * 32 + lane;  // key row within the tile (TMEM lane)
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + L::kTmemS + 64 * half;
+        const uint32_t dp_addr = tmem + lane_base + L::kTmemDP + 64 * half;
+        uint8_t* ds_panel = smem + L::kDS + half * kPanelBytes;
+        uint32_t g = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+            const BwdItem w = decode_bwd(idx, T, causal);
+            for (int it = 0; it < w.n; ++it, ++g) {
+                const int i = w.i0 + it;
+                const bool diag = causal && i == w.j;
+                if (!mbar_wait(&bars[L::kBarSdpFull], g & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                if (!mbar_wait(&bars[L::kBarDsFree], (g & 1) ^ 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                tc_fence_after();
+                const float* l2row = lse2 + (size_t)w.bh * N + (size_t)i * 128 + 64 * half;
+                const float* drow = delta + (size_t)w.bh * N + (size_t)i * 128 + 64 * half;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t s[32], dp[32];
+                    tmem_ld32(s_addr + 32 * c, s);
+                    tmem_ld32(dp_addr + 32 * c, dp);
+                    float lv[32], dv[32];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float4 a = __ldg(reinterpret_cast<const float4*>(l2row + 32 * c) + e);
+                        const float4 b = __ldg(reinterpret_cast<const float4*>(drow + 32 * c) + e);
+                        lv[4 * e] = a.x; lv[4 * e + 1] = a.y; lv[4 * e + 2] = a.z; lv[4 * e + 3] = a.w;
+                        dv[4 * e] = b.x; dv[4 * e + 1] = b.y; dv[4 * e + 2] = b.z; dv[4 * e + 3] = b.w;
+                    }
+                    tmem_wait_ld();
+                    uint32_t pk[16], dk16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int q0 = 64 * half + 32 * c + 2 * e;  // query column within the tile
+                        float p0 = ex2_ftz(fmaf(__uint_as_float(s[2 * e]), scale_log2, -lv[2 * e]));
+                        float p1 = ex2_ftz(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -lv[2 * e + 1]));
+                        if (diag) {
+                            // key row > query column is masked (P = dS = 0)
+                            if (row > q0) p0 = 0.f;
+                            if (row > q0 + 1) p1 = 0.f;
+                        }
+                        const float ds0 = p0 * (__uint_as_float(dp[2 * e]) - dv[2 * e]);
+                        const float ds1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1]);
+                        pk[e] = pack2<BF16>(p0, p1);
+                        dk16[e] = pack2<BF16>(ds0, ds1);
+                    }
+                    tmem_st16(s_addr + 16 * c, pk);
+                    tmem_st16(dp_addr + 16 * c, dk16);
+                    // dS^T row -> shared memory (128B-swizzled, MN-major A operand of dQ = dS K)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        uint4* dst = reinterpret_cast<uint4*>(ds_panel + sw128_offset(row, 4 * c + e));
+                        *dst = make_uint4(dk16[4 * e], dk16[4 * e + 1], dk16[4 * e + 2], dk16[4 * e + 3]);
+                    }
+                }
+                fence_proxy_async_smem();
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[L::kBarDsReady]);
+            }
+        }
+    } else if (warp < 12) {
+        regs_dec<112>();
+        // ------------------------------------------------------ dQ drain, dK/dV epilogue
+        const int row = (warp & 3) * 32 + lane;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        uint32_t g = 0;
+        int k = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+            const BwdItem w = decode_bwd(idx, T, causal);
+            for (int it = 0; it < w.n; ++it, ++g) {
+                const int i = w.i0 + it;
+                if (!mbar_wait(&bars[L::kBarDqFull], g & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                tc_fence_after();
+                float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tmem + lane_base + L::kTmemDQ + 32 * c, r);
+                    tmem_wait_ld();
+                    if (c == D / 32 - 1) {
+                        tc_fence_before();
+                        mbar_arrive(&bars[L::kBarDqFree]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        red_add_v4(dst + 32 * c + 4 * e, __uint_as_float(r[4 * e]) * scale,
+                                   __uint_as_float(r[4 * e + 1]) * scale, __uint_as_float(r[4 * e + 2]) * scale,
+                                   __uint_as_float(r[4 * e + 3]) * scale);
+                }
+            }
+            if (!ok) break;
+            if (!mbar_wait(&bars[L::kBarDkvFull], k & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+            tc_fence_after();
+            const size_t grow = (size_t)w.bh * N + (size_t)w.j * 128 + row;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t src = tmem + lane_base + (which ? L::kTmemDK : L::kTmemDV);
+                const float mul = which ? scale : 1.f;
+                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow * D * 2;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(src + c, r);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[L::kBarDkvEmpty]);
+        }
+    } else {
+        regs_dec<112>();  // warps 12-15; the split 2x144 + 112 + 112 warpgroups uses 65536 registers
+        if (warp == 12 && lane == 0) {
+            // ------------------------------------------------------ MMA issuer
+            constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
+            constexpr uint32_t kIdescG = idesc_f16(128, D, BF16, false, true);      // dV, dK (A in TMEM)
+            constexpr uint32_t kIdescQ = idesc_f16(128, D, BF16, true, true);       // dQ (A = dS, MN-major)
+            const uint32_t k_base = smem_u32(smem + L::kK), v_base = smem_u32(smem + L::kV);
+            const uint32_t q_base = smem_u32(smem + L::kQ), do_base = smem_u32(smem + L::kDO);
+            const uint32_t ds_base = smem_u32(smem + L::kDS);
+            uint32_t g = 0;
+            int k = 0;
+            bool ok = true;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+                const BwdItem w = decode_bwd(idx, T, causal);
+                if (!mbar_wait(&bars[L::kBarKVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                tc_fence_after();
+                for (int it = 0; it < w.n; ++it, ++g) {
+                    const uint32_t st = g & 1;
+                    if (!mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    if (!mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
+                    // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (both K-major operands)
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                        mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024),
+                               kIdescS, kk > 0);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                        mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(dos + off, 16, 1024),
+                               kIdescS, kk > 0);
+                    }
+                    mma_commit(&bars[L::kBarSdpFull]);
+                    if (!mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    if (it == 0 && !mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    tc_fence_after();
+                    // dV += P^T dO_i ; dK += dS^T Q_i  (A from TMEM, B = dO_i / Q_i MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+                        mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol, sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024),
+                               kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+                        mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol, sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024),
+                               kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(&bars[L::kBarQEmpty + st]);
+                    // dQ_i = dS K_j (A = dS from shared memory, MN-major; B = K_j MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + L::kTmemDQ, sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024),
+                               sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024), kIdescQ, kk > 0);
+                    mma_commit(&bars[L::kBarDqFull]);
+                    mma_commit(&bars[L::kBarDsFree]);
+                }
+                if (!ok) break;
+                mma_commit(&bars[L::kBarDkvFull]);
+                mma_commit(&bars[L::kBarKVEmpty]);
+            }
+            mma_commit(&bars[L::kBarTeardown]);
+            mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
+        } else if (warp == 13 && lane == 0) {
+            // ------------------------------------------------------ TMA producer
+            uint32_t g = 0;
+            int k = 0;
+            bool ok = true;
+            int issued_kv = -1;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+                const BwdItem w = decode_bwd(idx, T, causal);
+                if (!mbar_wait(&bars[L::kBarKVEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
+                mbar_arrive_expect_tx(&bars[L::kBarKVFull], 2 * L::kTile);
+                issued_kv = k;
+#pragma unroll
+                for (int p = 0; p < L::kPanels; ++p) {
+                    tma_load_3d(smem + L::kK + p * kPanelBytes, &tm_k, &bars[L::kBarKVFull], 64 * p, w.j * 128, w.bh);
+                    tma_load_3d(smem + L::kV + p * kPanelBytes, &tm_v, &bars[L::kBarKVFull], 64 * p, w.j * 128, w.bh);
+                }
+                for (int it = 0; it < w.n; ++it, ++g) {
+                    const int i = w.i0 + it;
+                    const uint32_t st = g & 1;
+                    if (!mbar_wait(&bars[L::kBarQEmpty + st], ((g >> 1) & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bars[L::kBarQFull + st], 2 * L::kTile);
+#pragma unroll
+                    for (int p = 0; p < L::kPanels; ++p) {
+                        tma_load_3d(smem + L::kQ + st * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + st],
+                                    64 * p, i * 128, w.bh);
+                        tma_load_3d(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
+                                    64 * p, i * 128, w.bh);
+                    }
+                }
+            }
+            // Let every copy issued above land before shared memory is released.
+            if (issued_kv >= 0) mbar_wait_drain(&bars[L::kBarKVFull], issued_kv & 1, kWaitLimitNs);
+            for (uint32_t t = (g > 2 ? g - 2 : 0); t < g; ++t)
+                mbar_wait_drain(&bars[L::kBarQFull + (t & 1)], (t >> 1) & 1, kWaitLimitNs);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 12) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+    using L = BwdLayout<D>;
+    const long rows = (long)a.BH * a.N;
+    // 1. preprocess
+    {
+        const long threads_needed = rows * (D / 8);
+        long blocks = (threads_needed + 255) / 256;
+        const long cap = (long)a.num_sms * 8;
+        if (blocks > cap) blocks = cap;
+        bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
+            static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, a.delta, a.lse2,
+            reinterpret_cast<float4*>(a.dq_acc), rows);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 2. main kernel
+    {
+        const int smem_bytes = L::kBytes + 1024;
+        auto kern = attn_bwd_kernel<D, BF16>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        if (e != cudaSuccess) return e;
+        const int T = a.N / 128;
+        const long n_items = (long)a.BH * T;
+        const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
+        kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc, a.dk,
+                                                      a.dv, a.BH, a.N, a.scale, a.causal, a.error);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 3. dQ conversion
+    {
+        const long n8 = rows * D / 8;
+        long blocks = (n8 + 255) / 256;
+        const long cap = (long)a.num_sms * 8;
+        if (blocks > cap) blocks = cap;
+        dq_convert_kernel<BF16><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
+                                                                 static_cast<uint4*>(a.dq), n8);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
+    if (a.d == 128) return a.fp16 ? launch_bwd_t<128, false>(a, stream) : launch_bwd_t<128, true>(a, stream);
+    if (a.d == 64) return a.fp16 ? launch_bwd_t<64, false>(a, stream) : launch_bwd_t<64, true>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gb300

@@ -1,0 +1,467 @@
+// Fused attention forward for sm_103a (tcgen05 + TMEM + TMA).
+//
+// Computes, per (batch, head), S = scale * Q K^T + M, the row log-sum-exp L,
+// P = exp(S - L) and O = P V without writing S or P to global memory
+// ("Writing Speed-of-Light Attention Backward Kernel for 5090 in CUDA",
+// section "Mathematical Formulation", forward equations).  The running-max
+// (online) softmax follows "Dense B200 attention from scratch" (b200-attention),
+// Chapter 1 section B; the kernel organisation (warp roles, two Q tiles per
+// CTA, a K/V ring, the peeled compute pipeline, base-2 exponentials with the
+// scale folded in, the lazy O rescale with threshold 8 and the separate
+// correction warps, persistent CTAs) follows its Chapters 4-8, 11, 12 and 14,
+// re-derived for sm_103a.  Causal tile skipping is added; that page's kernel
+// is non-causal.
+//
+// CTA layout (512 threads = 4 warpgroups):
+//   WG0 (warps 0-3)   softmax for Q tile 0 of the work item (row = thread)
+//   WG1 (warps 4-7)   softmax for Q tile 1
+//   WG2 (warps 8-11)  O correction (lazy rescale) and the epilogue
+//   WG3 warp 12       single-thread tcgen05.mma issuer (also owns TMEM)
+//   WG3 warp 13       TMA producer (Q tiles, K/V ring)
+//   WG3 warps 14-15   idle
+// TMEM (512 columns x 128 lanes): S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..).
+// Packed 16-bit P_q overwrites the first 64 columns of S_q.
+// Shared memory: Q0, Q1 (128 x d each) and a ring of K/V tiles (128 x d),
+// all in the 128-byte-swizzle layout written by TMA.
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace gb300 {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units (b200-attention, Chapter 11)
+constexpr int kPanelBytes = 128 * 128;     // 128 rows x 128 bytes (64 16-bit elements)
+
+template <int D>
+struct FwdLayout {
+    static constexpr int kTile = 128 * D * 2;          // bytes of a 128-row tile
+    static constexpr int kPanels = D / 64;
+    static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring depth
+    static constexpr int kQ0 = 0;
+    static constexpr int kQ1 = kTile;
+    static constexpr int kKV = 2 * kTile;
+    static constexpr int kAux = kKV + kStages * kTile;  // barriers and small arrays
+    // aux area
+    static constexpr int kBarQFull = 0, kBarQEmpty = 1;
+    static constexpr int kBarKVFull = 2;
+    static constexpr int kBarKVEmpty = kBarKVFull + kStages;
+    static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]
+    static constexpr int kBarPVReady = kBarSFull + 2;        // [2]
+    static constexpr int kBarODone = kBarPVReady + 2;        // [2]
+    static constexpr int kBarStats = kBarODone + 2;          // [2]
+    static constexpr int kBarFin = kBarStats + 2;            // [2 stages][2 buffers]
+    static constexpr int kBarTeardown = kBarFin + 4;
+    static constexpr int kNumBars = kBarTeardown + 1;
+    static constexpr int kScaleOff = kAux + 8 * 64;                // float [2][128]
+    static constexpr int kFinLOff = kScaleOff + 2 * 128 * 4;       // float [2 buf][2 q][128]
+    static constexpr int kFinMOff = kFinLOff + 4 * 128 * 4;        // float [2 buf][2 q][128]
+    static constexpr int kFinLqOff = kFinMOff + 4 * 128 * 4;       // float [2 buf][2 q][128]
+    static constexpr int kMiscOff = kFinLqOff + 4 * 128 * 4;       // tmem base, abort flag
+    static constexpr int kBytes = kMiscOff + 64;
+    static constexpr int kTmemS = 0;     // S_q at kTmemS + 128 q
+    static constexpr int kTmemO = 256;   // O_q at kTmemO + 128 q
+    static_assert(kNumBars <= 64, "barrier area");
+};
+
+struct WorkItem {
+    int bh, m;        // head index, Q tile pair index
+    int t0, t1;       // Q tile indices
+    int n0, n1;       // number of KV tiles for each Q tile
+};
+
+__device__ __forceinline__ WorkItem decode_item(int idx, int M, int T, int causal) {
+    WorkItem w;
+    w.bh = idx / M;
+    w.m = M - 1 - (idx % M);  // within a head, longest Q tile pair first
+    w.t0 = 2 * w.m;
+    w.t1 = 2 * w.m + 1;
+    w.n0 = causal ? min(w.t0 + 1, T) : T;
+    w.n1 = causal ? min(w.t1 + 1, T) : T;
+    return w;
+}
+
+template <int D, bool BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_out,
+                float* __restrict__ lse_out, int BH, int N, float scale, int causal, int* error) {
+    using L = FwdLayout<D>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Align the dynamic shared memory base to 1024 bytes (128B-swizzle atoms).
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kAux);
+    float* scale_buf = reinterpret_cast<float*>(smem + L::kScaleOff);
+    float* fin_l = reinterpret_cast<float*>(smem + L::kFinLOff);
+    float* fin_m = reinterpret_cast<float*>(smem + L::kFinMOff);
+    float* fin_lq = reinterpret_cast<float*>(smem + L::kFinLqOff);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
+    int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int T = N / 128;
+    const int M = (T + 1) / 2;
+    const int n_items = BH * M;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bars[L::kBarQFull], 1);
+        mbar_init(&bars[L::kBarQEmpty], 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&bars[L::kBarKVFull + s], 1);
+            mbar_init(&bars[L::kBarKVEmpty + s], 1);
+        }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&bars[L::kBarSFull + q], 1);
+            mbar_init(&bars[L::kBarPVReady + q], 256);  // 128 softmax + 128 correction threads
+            mbar_init(&bars[L::kBarODone + q], 1);
+            mbar_init(&bars[L::kBarStats + q], 128);
+            mbar_init(&bars[L::kBarFin + 2 * q + 0], 128);
+            mbar_init(&bars[L::kBarFin + 2 * q + 1], 128);
+        }
+        mbar_init(&bars[L::kBarTeardown], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 12) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    if (warp == 13 && lane == 0) {
+        prefetch_tensormap(&tm_q);
+        prefetch_tensormap(&tm_k);
+        prefetch_tensormap(&tm_v);
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const WaitGuard guard{abort_flag, error, kWaitLimitNs};
+    const float scale_log2 = scale * kLog2e;
+    const int wg = warp >> 2;
+
+    if (wg == 0 || wg == 1) {
+        // ------------------------------------------------------------ softmax
+        regs_inc<176>();
+        const int q = wg;
+        const int row = threadIdx.x & 127;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + L::kTmemS + 128 * q;
+        uint32_t s_phase = 0;
+        int k = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+            const WorkItem w = decode_item(idx, M, T, causal);
+            const int t = q ? w.t1 : w.t0;
+            const int n = q ? w.n1 : w.n0;
+            const int diag = (causal && t < T) ? t : -1;
+            float m_run = -INFINITY, l_run = 0.f, lq_run = 0.f;
+            for (int j = 0; j < n; ++j) {
+                if (!mbar_wait(&bars[L::kBarSFull + q], s_phase, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                s_phase ^= 1;
+                tc_fence_after();
+                uint32_t s[128];
+                tmem_ld32(s_addr + 0, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
+                tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
+                tmem_wait_ld();
+                if (j == diag) {
+                    // key index > query index is masked (aligned top-left causal mask)
+#pragma unroll
+                    for (int c = 0; c < 128; ++c)
+                        if (c > row) s[c] = __float_as_uint(-INFINITY);
+                }
+                float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+                for (int c = 0; c < 128; c += 8) {
+                    mx0 = fmax3(mx0, __uint_as_float(s[c + 0]), __uint_as_float(s[c + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(s[c + 2]), __uint_as_float(s[c + 3]));
+                    mx2 = fmax3(mx2, __uint_as_float(s[c + 4]), __uint_as_float(s[c + 5]));
+                    mx3 = fmax3(mx3, __uint_as_float(s[c + 6]), __uint_as_float(s[c + 7]));
+                }
+                const float tile_max = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scale_log2;
+                float alpha = 1.f;
+                if (j == 0) {
+                    m_run = tile_max;
+                } else if (tile_max - m_run > kRescaleThreshold) {
+                    alpha = ex2_ftz(m_run - tile_max);
+                    l_run *= alpha;
+                    lq_run *= alpha;
+                    m_run = tile_max;
+                }
+                scale_buf[q * 128 + row] = alpha;
+                mbar_arrive(&bars[L::kBarStats + q]);
+
+                // p = 2^(s * scale * log2(e) - m), rounded to 16 bits for the PV MMA.  Two row
+                // sums: l (exact p) gives L, lq (the rounded p the MMA actually uses) normalises
+                // O = (P V) / lq, so a dominant weight's rounding cancels in O.
+                const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+                const uint64_t nm2 = f2_pack(-m_run, -m_run);
+                uint64_t acc = 0, accq = 0;
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[32 * h + 2 * c]),
+                                                          __uint_as_float(s[32 * h + 2 * c + 1])), sl2, nm2);
+                        float x0, x1;
+                        f2_unpack(x, x0, x1);
+                        const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
+                        pk[c] = pack2<BF16>(p0, p1);
+                        acc = f2_add(acc, f2_pack(p0, p1));
+                        accq = f2_add(accq, unpack2<BF16>(pk[c]));
+                    }
+                    tmem_st16(s_addr + 16 * h, pk);
+                }
+                float sum0, sum1, sq0, sq1;
+                f2_unpack(acc, sum0, sum1);
+                f2_unpack(accq, sq0, sq1);
+                l_run += sum0 + sum1;
+                lq_run += sq0 + sq1;
+                if (j == n - 1) {
+                    const int b = k & 1;
+                    fin_l[(b * 2 + q) * 128 + row] = l_run;
+                    fin_lq[(b * 2 + q) * 128 + row] = lq_run;
+                    fin_m[(b * 2 + q) * 128 + row] = m_run;
+                    mbar_arrive(&bars[L::kBarFin + 2 * q + b]);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars[L::kBarPVReady + q]);
+            }
+        }
+    } else if (wg == 2) {
+        // ------------------------------------------------ correction + epilogue
+        regs_dec<72>();
+        const int row = threadIdx.x & 127;
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        uint32_t stats_phase[2] = {0, 0}, o_phase[2] = {0, 0};
+        int k = 0;
+        bool ok = true;
+        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+            const WorkItem w = decode_item(idx, M, T, causal);
+            for (int j = 0; j < w.n1 && ok; ++j) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int n = q ? w.n1 : w.n0;
+                    if (j >= n) continue;
+                    if (!mbar_wait(&bars[L::kBarStats + q], stats_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
+                    stats_phase[q] ^= 1;
+                    const float alpha = scale_buf[q * 128 + row];
+                    if (j > 0) {
+                        if (!mbar_wait(&bars[L::kBarODone + q], o_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
+                        o_phase[q] ^= 1;
+                        tc_fence_after();
+                        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                            const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
+#pragma unroll 1
+                            for (int c = 0; c < D; c += 32) {
+                                uint32_t r[32];
+                                tmem_ld32(o_addr + c, r);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+                                tmem_st32(o_addr + c, r);
+                            }
+                            tmem_wait_st();
+                        }
+                    }
+                    tc_fence_before();
+                    mbar_arrive(&bars[L::kBarPVReady + q]);
+                }
+            }
+            if (!ok) break;
+            // epilogue: O = O / l -> 16-bit, L = (m + log2 l) ln 2
+            for (int q = 0; q < 2 && ok; ++q) {
+                const int b = k & 1;
+                if (!mbar_wait(&bars[L::kBarODone + q], o_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
+                o_phase[q] ^= 1;
+                if (!mbar_wait(&bars[L::kBarFin + 2 * q + b], (k >> 1) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                tc_fence_after();
+                const float l = fin_l[(b * 2 + q) * 128 + row];
+                const float lq = fin_lq[(b * 2 + q) * 128 + row];
+                const float mrow = fin_m[(b * 2 + q) * 128 + row];
+                const int t = q ? w.t1 : w.t0;
+                const int grow = t * 128 + row;
+                const float inv_l = 1.f / lq;
+                const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
+                uint8_t* dst = reinterpret_cast<uint8_t*>(o_out) + ((size_t)w.bh * N + grow) * (size_t)D * 2;
+#pragma unroll 1
+                for (int c = 0; c < D; c += 32) {
+                    uint32_t r[32];
+                    tmem_ld32(o_addr + c, r);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
+                    if (t < T) {
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
+                }
+                if (t < T) lse_out[(size_t)w.bh * N + grow] = (mrow + log2f(l)) * kLn2;
+                tc_fence_before();
+            }
+        }
+    } else {
+        regs_dec<88>();  // warps 12-15; the split 2x176 + 72 + 88 warpgroups uses 65536 registers
+        if (warp == 12 && lane == 0) {
+            // ------------------------------------------------------------ MMA issuer
+            constexpr uint32_t kIdescQK = idesc_f16(128, 128, BF16, false, false);
+            constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, false, true);
+            const uint32_t q_base[2] = {smem_u32(smem + L::kQ0), smem_u32(smem + L::kQ1)};
+            const uint32_t kv_base = smem_u32(smem + L::kKV);
+            uint32_t tok = 0, q_phase = 0, pv_phase[2] = {0, 0};
+            bool ok = true;
+            auto issue_qk = [&](int q, uint32_t slot) {
+                const uint32_t d_tmem = tmem + L::kTmemS + 128 * q;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                    const uint64_t a = sdesc_sw128(q_base[q] + off, 16, 1024);
+                    const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + off, 16, 1024);
+                    mma_ss(d_tmem, a, b, kIdescQK, kk > 0);
+                }
+            };
+            auto issue_pv = [&](int q, uint32_t slot, bool acc) {
+                const uint32_t d_tmem = tmem + L::kTmemO + 128 * q;
+                const uint32_t p_tmem = tmem + L::kTmemS + 128 * q;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + kk * 2048, kPanelBytes, 1024);
+                    mma_ts(d_tmem, p_tmem + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto wait_kv = [&](uint32_t& slot) -> bool {
+                slot = tok % L::kStages;
+                const bool r = mbar_wait(&bars[L::kBarKVFull + slot], (tok / L::kStages) & 1, guard, kDevTimeoutMma);
+                ++tok;
+                tc_fence_after();
+                return r;
+            };
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
+                const WorkItem w = decode_item(idx, M, T, causal);
+                if (!mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
+                q_phase ^= 1;
+                tc_fence_after();
+                uint32_t kslot;
+                if (!wait_kv(kslot)) { ok = false; break; }
+                issue_qk(0, kslot);
+                mma_commit(&bars[L::kBarSFull + 0]);
+                issue_qk(1, kslot);
+                mma_commit(&bars[L::kBarSFull + 1]);
+                mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                for (int j = 0; j < w.n1 && ok; ++j) {
+                    uint32_t vslot;
+                    if (!wait_kv(vslot)) { ok = false; break; }
+                    bool have_k = false;
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const int n = q ? w.n1 : w.n0;
+                        if (j >= n) continue;
+                        if (!mbar_wait(&bars[L::kBarPVReady + q], pv_phase[q], guard, kDevTimeoutMma)) { ok = false; break; }
+                        pv_phase[q] ^= 1;
+                        tc_fence_after();
+                        issue_pv(q, vslot, j > 0);
+                        mma_commit(&bars[L::kBarODone + q]);
+                        if (j + 1 < n) {
+                            if (!have_k) {
+                                if (!wait_kv(kslot)) { ok = false; break; }
+                                have_k = true;
+                            }
+                            issue_qk(q, kslot);
+                            mma_commit(&bars[L::kBarSFull + q]);
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&bars[L::kBarKVEmpty + vslot]);
+                    if (have_k) mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                }
+                mma_commit(&bars[L::kBarQEmpty]);
+            }
+            // Every MMA issued above completes before TMEM is released.
+            mma_commit(&bars[L::kBarTeardown]);
+            mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
+        } else if (warp == 13 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer
+            uint32_t tok = 0;
+            int k = 0;
+            bool ok = true;
+            int last_q_item = -1;
+            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
+                const WorkItem w = decode_item(idx, M, T, causal);
+                if (k > 0 && !mbar_wait(&bars[L::kBarQEmpty], (k - 1) & 1, guard, kDevTimeoutLoad)) { ok = false; break; }
+                mbar_arrive_expect_tx(&bars[L::kBarQFull], 2 * L::kTile);
+                last_q_item = k;
+#pragma unroll
+                for (int p = 0; p < L::kPanels; ++p) {
+                    tma_load_3d(smem + L::kQ0 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t0 * 128, w.bh);
+                    tma_load_3d(smem + L::kQ1 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t1 * 128, w.bh);
+                }
+                for (int j = 0; j < w.n1 && ok; ++j) {
+#pragma unroll
+                    for (int which = 0; which < 2; ++which) {
+                        const uint32_t slot = tok % L::kStages;
+                        if (tok >= (uint32_t)L::kStages &&
+                            !mbar_wait(&bars[L::kBarKVEmpty + slot], ((tok / L::kStages) - 1) & 1, guard, kDevTimeoutLoad)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&bars[L::kBarKVFull + slot], L::kTile);
+                        const CUtensorMap* map = which ? &tm_v : &tm_k;
+#pragma unroll
+                        for (int p = 0; p < L::kPanels; ++p)
+                            tma_load_3d(smem + L::kKV + slot * L::kTile + p * kPanelBytes, map,
+                                        &bars[L::kBarKVFull + slot], 64 * p, j * 128, w.bh);
+                        ++tok;
+                    }
+                }
+            }
+            // Let every copy issued above land before shared memory is released.
+            if (last_q_item >= 0) mbar_wait_drain(&bars[L::kBarQFull], last_q_item & 1, kWaitLimitNs);
+            for (uint32_t t = (tok > (uint32_t)L::kStages ? tok - L::kStages : 0); t < tok; ++t)
+                mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 12) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16>
+cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
+    using L = FwdLayout<D>;
+    const int smem_bytes = L::kBytes + 1024;  // + alignment slack
+    auto kern = attn_fwd_kernel<D, BF16>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e != cudaSuccess) return e;
+    const int T = a.N / 128;
+    const int M = (T + 1) / 2;
+    const long n_items = (long)a.BH * M;
+    const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
+    if (grid <= 0) return cudaSuccess;
+    kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.BH, a.N, a.scale,
+                                                  a.causal, a.error);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
+    if (a.d == 128) return a.fp16 ? launch_fwd_t<128, false>(a, stream) : launch_fwd_t<128, true>(a, stream);
+    if (a.d == 64) return a.fp16 ? launch_fwd_t<64, false>(a, stream) : launch_fwd_t<64, true>(a, stream);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace gb300

@@ -1,0 +1,120 @@
+/*
+ * attn.h - C ABI of the GB300 (sm_103a) fused exact-attention library
+ * (libattn_gb300.so).
+ *
+ * The operations are those of "Writing Speed-of-Light Attention Backward
+ * Kernel for 5090 in CUDA", section "Mathematical Formulation":
+ *
+ *   forward   S = scale * Q K^T + M,  L_i = log sum_j exp(S_ij),
+ *             P = exp(S - L),  O = P V
+ *   backward  D = rowsum(dO o O),  dV = P^T dO,  dP = dO V^T,
+ *             dS = P o (dP - D 1^T),  dQ = scale * dS K,  dK = scale * dS^T Q
+ *
+ * where M_ij = -inf for key j > query i when `causal` is non-zero (the
+ * diagonal is kept) and 0 otherwise.  The page writes 1/sqrt(d) for the
+ * scale; here it is the caller's `scale`.  S and P are never written to
+ * global memory: the backward recomputes P from the saved L.
+ *
+ * Conventions shared by every call
+ *  - All tensor pointers are DEVICE pointers, owned by the caller, allocated
+ *    on the current CUDA device.  The library allocates no device memory.
+ *  - Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays of 16-bit
+ *    floats (bfloat16, or float16 for the *_ex calls with ATTN_FP16), row
+ *    d fastest.  L (lse) is a contiguous FP32 [B, H, N] array, natural log.
+ *  - Supported sizes: d in {64, 128}; N >= 128 and N % 128 == 0; B, H >= 1;
+ *    B*H*N*d < 2^31.  Every pointer must be 16-byte aligned.  Anything else
+ *    returns an error code before any work is queued.
+ *  - Outputs are overwritten, never accumulated.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *    default stream).  A status of ATTN_OK means the work was queued.  Launch
+ *    failures are reported as ATTN_ERR_CUDA.  A kernel whose internal wait
+ *    gave up (it never should) records that in a device error word, which
+ *    attn_last_device_error() reads back.
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef ATTN_GB300_H
+#define ATTN_GB300_H
+
+#include <stddef.h>
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad dtype   */
+    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, N % 128 != 0, too large  */
+    ATTN_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned                */
+    ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required      */
+    ATTN_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed             */
+    ATTN_ERR_TIMEOUT = 6       /* a kernel-internal wait gave up (device word) */
+} attn_status_t;
+
+typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
+
+/*
+ * Forward pass (the page's forward equations, section "Mathematical
+ * Formulation").  Reads q, k, v [B,H,N,d]; writes o [B,H,N,d] and
+ * lse [B,H,N] (L, natural log, FP32), which attn_bwd needs.  BF16 data.
+ */
+ATTN_API attn_status_t attn_fwd(const void *q, const void *k, const void *v, void *o, float *lse,
+                       int B, int H, int N, int d, float scale, int causal, void *stream);
+
+/* attn_fwd with an explicit 16-bit element type (ATTN_BF16 or ATTN_FP16). */
+ATTN_API attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
+                          int B, int H, int N, int d, float scale, int causal,
+                          attn_dtype_t dtype, void *stream);
+
+/*
+ * Bytes of device workspace attn_bwd needs: the D vector and L*log2(e)
+ * (FP32 [B,H,N] each) and the FP32 dQ accumulator [B,H,N,d].  Returns 0 for
+ * sizes attn_bwd would reject.
+ */
+ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * Backward pass (the page's backward equations, section "Mathematical
+ * Formulation", with the tiling of its pseudocode: parallel over key/value
+ * tiles, dQ partials combined in FP32).  Reads q, k, v, o, dout [B,H,N,d]
+ * and lse [B,H,N] as written by attn_fwd for the same q, k, v, scale and
+ * causal; writes dq, dk, dv [B,H,N,d].  `workspace` is caller-owned device
+ * memory of at least attn_bwd_workspace_size() bytes, 256-byte aligned; its
+ * contents on entry do not matter and are clobbered.
+ */
+ATTN_API attn_status_t attn_bwd(const void *q, const void *k, const void *v, const void *o,
+                       const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                       void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                       float scale, int causal, void *stream);
+
+/* attn_bwd with an explicit 16-bit element type. */
+ATTN_API attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, const void *o,
+                          const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                          void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                          float scale, int causal, attn_dtype_t dtype, void *stream);
+
+/* Static string naming a status code. */
+ATTN_API const char *attn_status_string(attn_status_t status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel wait gave up;
+ * its outputs are incomplete) or ATTN_ERR_CUDA (the synchronisation failed).
+ */
+ATTN_API attn_status_t attn_last_device_error(void *stream);
+
+/* Number of kernel launches the most recent attn_fwd* / attn_bwd* call on
+ * this host thread queued (0 after a rejected call). */
+ATTN_API int attn_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_GB300_H */

@@ -1,0 +1,68 @@
+"""The C-ABI library loads and exports every symbol include/attn.h declares;
+argument checks that run before any CUDA call return the documented codes.
+No kernel is launched here (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import shutil
+    from exact_attention_flashattention_gb300 import build as b
+    if not os.path.exists(b.LIB):
+        if shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"):
+            pytest.skip("nvcc not available to build the library")
+        b.build()
+    import exact_attention_flashattention_gb300 as attn
+    return attn.load()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(attn_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("attn_fwd", "attn_fwd_ex", "attn_bwd", "attn_bwd_ex", "attn_bwd_workspace_size",
+              "attn_status_string", "attn_last_device_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_names_match_exports():
+    import exact_attention_flashattention_gb300 as attn
+    assert set(attn.EXPORTS) <= set(declared_functions())
+
+
+def test_argument_checks_before_any_launch(lib):
+    import exact_attention_flashattention_gb300 as attn
+    vp = ctypes.c_void_p
+    p = vp(256)  # never dereferenced: every case below is rejected first
+    null = vp(0)
+    assert lib.attn_fwd(null, p, p, p, p, 1, 1, 128, 128, 1.0, 1, null) == 1          # INVALID_ARG
+    assert lib.attn_fwd(p, p, p, p, p, 1, 1, 128, 96, 1.0, 1, null) == 2              # d unsupported
+    assert lib.attn_fwd(p, p, p, p, p, 1, 1, 100, 128, 1.0, 1, null) == 2             # N % 128
+    assert lib.attn_fwd(p, p, p, p, p, 0, 1, 128, 128, 1.0, 1, null) == 1             # B <= 0
+    assert lib.attn_fwd(vp(258), p, p, p, p, 1, 1, 128, 128, 1.0, 1, null) == 3       # alignment
+    assert lib.attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 128, 1.0, 1, 7, null) == 1       # bad dtype
+    ws = attn.attn_bwd_workspace_size(1, 1, 128, 128)
+    assert ws >= 128 * 4 * 2 + 128 * 128 * 4 and ws % 256 == 0
+    assert attn.attn_bwd_workspace_size(1, 1, 100, 128) == 0
+    assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, null, 0, 1, 1, 128, 128, 1.0, 1, null) == 4   # workspace
+    assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, vp(512), ws - 1, 1, 1, 128, 128, 1.0, 1, null) == 4
+    assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, vp(512 + 16), ws, 1, 1, 128, 128, 1.0, 1, null) == 3
+    assert lib.attn_last_launch_count() == 0
+    for s in range(7):
+        assert attn.attn_status_string(s).startswith("ATTN_")
