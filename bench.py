@@ -1,0 +1,434 @@
+#!/usr/bin/env python
+"""Benchmark: exact fused attention forward + backward on GB300 (sm_103a).
+
+One step = one forward (attn_fwd) and one backward (attn_bwd: preprocess, main
+kernel, dQ conversion) over the causal BF16 workload B=8, H=16, N=4096, d=128,
+scale 1/sqrt(128), inputs ~ N(0, 1).  Prints ONE JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+value        whole-job TFLOPS of the step, FLOP convention fwd 4 B H N^2 d and
+             bwd 10 B H N^2 d, each halved for causal; inputs resident in HBM.
+e2e          the same metric through the C ABI with HOST (pinned) buffers:
+             q, k, v, dO copied in and o, lse, dq, dk, dv copied out every step.
+roofline     the backward main kernel (the dominant one): its algorithmic FLOPs
+             per launch / its CUDA-event duration, against the measured
+             sustained bf16 peak; traffic from a committed ncu capture when it
+             matches the current kernel source, else null.
+cpu_baseline the FP64 oracle, as it stands, on a bounded sample of the same
+             workload on this host's cores (rank 0, N=1 only).
+--impl reference  times that oracle alone, each step a bounded sample.
+
+Multi-GPU (torchrun): every rank runs its own copy of the workload (heads are
+independent, no data-path collective); value = all ranks' FLOPs / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd / bwd TFLOPS (BF16, d=128, causal) and % of GB300 BF16 peak"
+WORKLOAD = dict(B=8, H=16, N=4096, d=128, causal=True)
+WORKLOAD_NAME = "causal MHA BF16 fwd+bwd B=8 H=16 N=4096 d=128, scale 1/sqrt(128), q,k,v,dO ~ N(0,1)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_flashattention_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel_key):
+    """DRAM bytes per launch from profiles/traffic.json, if it was taken on the
+    current kernel source (same sha); otherwise None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel_key)
+    if not e or e.get("source_sha") != kernel_source_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- oracle sample
+def oracle_sample(n_heads, rows_per_head, seed=4242):
+    """Time the FP64 oracle on a bounded sample of the workload: n_heads heads,
+    each restricted to rows_per_head query rows spread evenly over [0, N) (so the
+    causal work per row averages that of the whole head).  One head per thread.
+    Returns (seconds, algorithmic FLOPs of the sample, threads)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    import oracle
+    import seeded_inputs as si
+
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    scale = d ** -0.5
+    heads = [(h * 37) % (B * H) for h in range(n_heads)]
+    data = {n: si.tensor_heads(seed, n, B * H, N, d, 1.0, heads=heads) for n in ("q", "k", "v", "do")}
+    stride = max(1, N // rows_per_head)
+    rows = np.arange(stride // 2, N, stride)[:rows_per_head]
+    f64 = [{n: si.bits_to_f32(data[n][i], "bf16").astype(np.float64) for n in data} for i in range(n_heads)]
+    oracle.build()
+
+    def one(i):
+        x = f64[i]
+        oracle.attn_bwd_rowset(x["q"], x["k"], x["v"], x["do"], rows, scale, causal)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(n_heads) as ex:
+        list(ex.map(one, range(n_heads)))
+    dt = time.perf_counter() - t0
+    # pages' convention: 14 d FLOPs (fwd 4 d + bwd 10 d) per unmasked (query, key) pair
+    pairs = float(np.sum(rows + 1)) if causal else float(len(rows) * N)
+    flops = 14.0 * d * pairs * n_heads
+    return dt, flops, n_heads
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    cores = host_cores()
+    n_heads = min(cores, 16)
+    rows = 64
+    for _ in range(args.warmup):
+        oracle_sample(n_heads, rows)
+    times, flops = [], 0.0
+    for _ in range(args.steps):
+        dt, fl, _ = oracle_sample(n_heads, rows)
+        times.append(dt)
+        flops = fl
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    sample = (f"{n_heads} heads x {rows} query rows (rows spread evenly over N) of the {WORKLOAD_NAME} "
+              f"workload, full fwd+bwd work of those rows, per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": n_heads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args):
+    import torch
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_flashattention_gb300 as attn
+    from exact_attention_flashattention_gb300 import flops as F
+
+    B, H, N, d, causal = (WORKLOAD[k] for k in ("B", "H", "N", "d", "causal"))
+    scale = d ** -0.5
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234 + rank)
+    shape = (B, H, N, d)
+    q, k, v, do = (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                   for _ in range(4))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    fwd_fl = F.fwd_flops(B, H, N, d, causal)
+    bwd_fl = F.bwd_flops(B, H, N, d, causal)
+    launches_per_step = 4  # forward kernel + preprocess + backward main + dQ conversion
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        attn.attn_fwd(q, k, v, o, lse, scale, causal, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        attn.attn_bwd_stage(0, q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        attn.attn_bwd_stage(1, q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        attn.attn_bwd_stage(2, q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    if attn.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    if attn.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set during the timed region")
+
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
+    fwd_med = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    bwd_med = statistics.median(e[1].elapsed_time(e[4]) for e in evs)
+    ms_per_step = max_over_ranks(total_ms / args.steps, world)
+    value = (fwd_fl + bwd_fl) * world / ms_per_step / 1e9
+
+    # ---- end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        pin = {n: t.cpu().pin_memory() for n, t in (("q", q), ("k", k), ("v", v), ("do", do))}
+        outs = {n: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = sum(t.numel() * t.element_size() for t in outs.values())
+
+        def e2e_step():
+            q.copy_(pin["q"], non_blocking=True)
+            k.copy_(pin["k"], non_blocking=True)
+            v.copy_(pin["v"], non_blocking=True)
+            do.copy_(pin["do"], non_blocking=True)
+            attn.attn_fwd(q, k, v, o, lse, scale, causal, stream)
+            attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal, stream)
+            for n, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+                outs[n].copy_(t, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        n_e2e = max(3, min(args.steps, 20))
+        barrier(world)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        e2e_ms = max_over_ranks(a.elapsed_time(b) / n_e2e, world)
+        e2e = {"value": (fwd_fl + bwd_fl) * world / e2e_ms / 1e9, "unit": "TFLOPS", "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    main_tflops = bwd_fl / main_ms / 1e9
+    traffic = committed_traffic("attn_bwd_kernel<128,bf16>")
+    fwd_tf = fwd_fl / fwd_med / 1e9
+    bwd_tf = bwd_fl / bwd_med / 1e9
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_heads = min(host_cores(), 16)
+        rows = 2048
+        dt, fl, thr = oracle_sample(n_heads, rows)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": thr, "kind": "oracle",
+               "sample": f"{n_heads} heads x {rows} query rows (spread evenly over N) of the same workload, "
+                         f"full fwd+bwd work of those rows, {dt:.1f} s wall",
+               "seconds": dt}
+
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOPS",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (q, k, v, dO: 134 MB each; 129 MB L2), no flush"},
+        "fwd_tflops": fwd_tf,
+        "bwd_tflops": bwd_tf,
+        "fwd_pct_peak": 100.0 * fwd_tf / peak_burst,
+        "bwd_pct_peak": 100.0 * bwd_tf / peak_burst,
+        "pct_peak_basis": f"bf16_tflops (burst) = {peak_burst} TFLOP/s, {peak_src}",
+        "kernel_ms": {"attn_fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms, "bwd_dq_convert": conv_ms},
+        "roofline": {
+            "kernel": "attn_bwd_kernel<128,bf16> (backward main)",
+            "bound": "tensor",
+            "achieved": main_tflops,
+            "peak": peak_sus,
+            "unit": "TFLOP/s",
+            "frac": main_tflops / peak_sus,
+            "peak_kind": f"bf16_tflops_sustained, {peak_src}",
+            "traffic": traffic,
+            "algorithmic_flops_per_launch": bwd_fl,
+        },
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--shape", default=None,
+                    help="B,H,N,d[,noncausal] instead of the default workload (smaller cases for profiling)")
+    args = ap.parse_args()
+    if args.shape:
+        parts = args.shape.split(",")
+        WORKLOAD.update(B=int(parts[0]), H=int(parts[1]), N=int(parts[2]), d=int(parts[3]),
+                        causal=not (len(parts) > 4 and parts[4] == "noncausal"))
+        global WORKLOAD_NAME
+        WORKLOAD_NAME = ("{} MHA BF16 fwd+bwd B={B} H={H} N={N} d={d}, q,k,v,dO ~ N(0,1)"
+                         .format("causal" if WORKLOAD["causal"] else "non-causal", **WORKLOAD))
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -20,7 +20,7 @@ import os
 import threading
 
 __all__ = [
-    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_last_device_error",
+    "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_stage", "attn_bwd_workspace_size", "attn_last_device_error",
     "attn_status_string", "attn_last_launch_count", "forward", "backward", "library_path", "load",
 ]
 
@@ -33,7 +33,7 @@ ATTN_OK = 0
 ATTN_BF16, ATTN_FP16 = 0, 1
 
 EXPORTS = (
-    "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex",
+    "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex", "attn_bwd_stage",
     "attn_status_string", "attn_last_device_error", "attn_last_launch_count",
 )
 
@@ -64,13 +64,15 @@ def load():
         lib.attn_fwd_ex.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, vp]
         lib.attn_bwd.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, vp]
         lib.attn_bwd_ex.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, vp]
+        lib.attn_bwd_stage.argtypes = [i] + [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, vp]
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_last_device_error.argtypes = [vp]
         lib.attn_last_launch_count.argtypes = []
-        for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_last_device_error,
+        for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_bwd_stage,
+                   lib.attn_last_device_error,
                    lib.attn_last_launch_count):
             fn.restype = ctypes.c_int
         _lib = lib
@@ -130,6 +132,20 @@ def attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal:
                          B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
+
+
+def attn_bwd_stage(stage: int, q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool,
+                   stream=None) -> None:
+    """Queue one of the three backward kernels (0 preprocess, 1 main, 2 dQ convert)."""
+    lib = load()
+    B, H, N, d = q.shape
+    st = lib.attn_bwd_stage(int(stage), _check(q, "q"), _check(k, "k"), _check(v, "v"), _check(o, "o"),
+                            _check(dout, "dout"), _check(lse, "lse"), _check(dq, "dq"), _check(dk, "dk"),
+                            _check(dv, "dv"), _check(workspace, "workspace"),
+                            workspace.numel() * workspace.element_size(), B, H, N, d, float(scale),
+                            int(bool(causal)), _dtype_code(q), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, f"attn_bwd_stage({stage})")
 
 
 def attn_last_device_error(stream=None) -> int:

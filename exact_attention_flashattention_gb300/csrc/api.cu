@@ -146,10 +146,14 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
     return ws_layout(B, H, N, d).total;
 }
 
-attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                          const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                          int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+attn_status_t bwd_common(int stage, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                         int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
     t_last_launches = 0;
+    if (stage < -1 || stage > 2) return ATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
     attn_status_t st = check_sizes(B, H, N, d);
@@ -186,9 +190,31 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
     a.fp16 = dtype == ATTN_FP16;
     a.num_sms = di.sms;
     a.error = di.err_ptr;
-    if (launch_bwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-    t_last_launches = 3;
+    if (launch_bwd(a, static_cast<cudaStream_t>(stream), stage) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_launches = stage < 0 ? 3 : 1;
     return ATTN_OK;
+}
+}  // namespace
+
+extern "C" {
+
+attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
+                          int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+    return bwd_common(-1, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
+                      dtype, stream);
+}
+
+attn_status_t attn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                             size_t workspace_bytes, int B, int H, int N, int d, float scale, int causal,
+                             attn_dtype_t dtype, void* stream) {
+    if (stage < 0 || stage > 2) {
+        t_last_launches = 0;
+        return ATTN_ERR_INVALID_ARG;
+    }
+    return bwd_common(stage, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
+                      causal, dtype, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -410,11 +410,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 }
 
 template <int D, bool BF16>
-cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
+cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     using L = BwdLayout<D>;
     const long rows = (long)a.BH * a.N;
     // 1. preprocess
-    {
+    if (stage < 0 || stage == 0) {
         const long threads_needed = rows * (D / 8);
         long blocks = (threads_needed + 255) / 256;
         const long cap = (long)a.num_sms * 8;
@@ -426,7 +426,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     // 2. main kernel
-    {
+    if (stage < 0 || stage == 1) {
         const int smem_bytes = L::kBytes + 1024;
         auto kern = attn_bwd_kernel<D, BF16>;
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
@@ -440,22 +440,26 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
     }
     // 3. dQ conversion
-    {
+    if (stage < 0 || stage == 2) {
         const long n8 = rows * D / 8;
         long blocks = (n8 + 255) / 256;
         const long cap = (long)a.num_sms * 8;
         if (blocks > cap) blocks = cap;
         dq_convert_kernel<BF16><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
                                                                  static_cast<uint4*>(a.dq), n8);
-        return cudaGetLastError();
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
+    return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream) {
-    if (a.d == 128) return a.fp16 ? launch_bwd_t<128, false>(a, stream) : launch_bwd_t<128, true>(a, stream);
-    if (a.d == 64) return a.fp16 ? launch_bwd_t<64, false>(a, stream) : launch_bwd_t<64, true>(a, stream);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage) {
+    if (a.d == 128)
+        return a.fp16 ? launch_bwd_t<128, false>(a, stream, stage) : launch_bwd_t<128, true>(a, stream, stage);
+    if (a.d == 64)
+        return a.fp16 ? launch_bwd_t<64, false>(a, stream, stage) : launch_bwd_t<64, true>(a, stream, stage);
     return cudaErrorInvalidValue;
 }
 

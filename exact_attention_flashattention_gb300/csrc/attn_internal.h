@@ -53,6 +53,7 @@ struct BwdArgs {
 };
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
-cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream);
+// stage: -1 = all three kernels; 0 = preprocess; 1 = main kernel; 2 = dQ conversion.
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage);
 
 }  // namespace gb300

@@ -99,6 +99,21 @@ ATTN_API attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, 
                           void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
                           float scale, int causal, attn_dtype_t dtype, void *stream);
 
+/*
+ * The three kernels attn_bwd_ex queues, one at a time, for callers that time
+ * them separately or interleave other work on the stream.  stage 0: the
+ * preprocess (D = rowsum(dO o O), L log2(e), zeroing the FP32 dQ
+ * accumulator); stage 1: the main kernel (dK, dV, and the dQ partials added
+ * into the accumulator); stage 2: conversion of the accumulator to dq.
+ * Arguments as attn_bwd_ex; the workspace must persist across the three
+ * calls.  Queuing stages 0, 1, 2 in that order on one stream is exactly one
+ * attn_bwd_ex call.  Any other stage value returns ATTN_ERR_INVALID_ARG.
+ */
+ATTN_API attn_status_t attn_bwd_stage(int stage, const void *q, const void *k, const void *v,
+                             const void *o, const void *dout, const float *lse, void *dq, void *dk,
+                             void *dv, void *workspace, size_t workspace_bytes, int B, int H, int N,
+                             int d, float scale, int causal, attn_dtype_t dtype, void *stream);
+
 /* Static string naming a status code. */
 ATTN_API const char *attn_status_string(attn_status_t status);
 

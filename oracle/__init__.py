@@ -60,8 +60,9 @@ def load_library(path: str):
     lib.oracle_attn_bwd.argtypes = [L, L, L, D, I, dp, dp, dp, dp, dp, dp, dp, dp, dp, dp]
     lib.oracle_attn_rows.argtypes = [L, L, D, I, dp, dp, dp, dp, L, lp, dp, dp, dp]
     lib.oracle_attn_probs.argtypes = [L, L, D, I, dp, dp, dp, dp, dp, dp]
+    lib.oracle_attn_bwd_rowset.argtypes = [L, L, D, I, dp, dp, dp, dp, L, lp, dp, dp, dp]
     for f in (lib.oracle_attn_fwd, lib.oracle_attn_bwd, lib.oracle_attn_rows,
-              lib.oracle_attn_probs):
+              lib.oracle_attn_probs, lib.oracle_attn_bwd_rowset):
         f.restype = ctypes.c_int
     lib.oracle_num_threads.argtypes = []
     lib.oracle_num_threads.restype = ctypes.c_int
@@ -166,6 +167,25 @@ def attn_rows(q, k, v, rows, scale: float, causal: bool, dout=None):
     if rc != 0:
         raise RuntimeError(f"oracle_attn_rows failed ({rc})")
     return o, lse, dq
+
+
+def attn_bwd_rowset(q, k, v, dout, rows, scale: float, causal: bool):
+    """Forward + backward of ONE head ([N, d] inputs) restricted to query rows
+    `rows`: returns (dQ_rows [n, d], dK_part [N, d], dV_part [N, d]) where the
+    parts are those rows' contributions to dK and dV.  Single-threaded."""
+    lib = _load()
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    N, d = q.shape
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    n = rows.shape[0]
+    dq = np.empty((n, d), dtype=np.float64)
+    dk = np.empty((N, d), dtype=np.float64)
+    dv = np.empty((N, d), dtype=np.float64)
+    rc = lib.oracle_attn_bwd_rowset(N, d, float(scale), int(bool(causal)), _ptr(q), _ptr(k), _ptr(v), _ptr(dout),
+                                    n, rows.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_bwd_rowset failed ({rc})")
+    return dq, dk, dv
 
 
 def attn_probs(q, k, v, scale: float, causal: bool, dout=None):

@@ -223,6 +223,46 @@ int oracle_attn_rows(long N, long d, double scale, int causal,
 }
 
 /*
+ * Forward and backward restricted to the listed query rows of ONE head: the
+ * same per-row work as oracle_attn_bwd, for rows[0..nrows) only.  dq_rows
+ * [nrows, d] gets dQ_i; dk_part and dv_part [N, d] get the contributions of
+ * just these rows to dK and dV (the sums over i of oracle_attn_bwd, restricted
+ * to the listed i).  Used to time a bounded, representative sample of a large
+ * workload; not parallel (callers run one head per thread).
+ */
+int oracle_attn_bwd_rowset(long N, long d, double scale, int causal,
+                           const double *q, const double *k, const double *v,
+                           const double *dout, long nrows, const long *rows,
+                           double *dq_rows, double *dk_part, double *dv_part)
+{
+    if (bad_sizes(1, N, d) || nrows < 0) return -1;
+    for (long r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+    size_t n1 = (size_t)(N ? N : 1);
+    double *s = malloc(sizeof(double) * n1);
+    double *p = malloc(sizeof(double) * n1);
+    double *ds = malloc(sizeof(double) * n1);
+    double *o_i = malloc(sizeof(double) * (size_t)d);
+    if (!s || !p || !ds || !o_i) { free(s); free(p); free(ds); free(o_i); return -2; }
+    memset(dk_part, 0, sizeof(double) * (size_t)(N * d));
+    memset(dv_part, 0, sizeof(double) * (size_t)(N * d));
+    for (long r = 0; r < nrows; ++r) {
+        long i = rows[r];
+        double L, D;
+        forward_row(q, k, v, N, d, scale, causal, i, s, p, o_i, &L);
+        backward_row(q, k, v, dout, N, d, scale, i, p, o_i, ds, dq_rows + r * d, &D);
+        for (long j = 0; j < N; ++j) {
+            if (p[j] != 0.0)
+                for (long c = 0; c < d; ++c) dv_part[j * d + c] += p[j] * dout[i * d + c];
+            if (ds[j] != 0.0)
+                for (long c = 0; c < d; ++c) dk_part[j * d + c] += scale * ds[j] * q[i * d + c];
+        }
+    }
+    free(s); free(p); free(ds); free(o_i);
+    return 0;
+}
+
+/*
  * Whole P and dS matrices of one head ([N, N] each), for invariant checks on
  * tiny inputs.  dout may be NULL, in which case ds is not written.
  */

@@ -193,6 +193,22 @@ def test_row_entry_point_matches_whole_head(causal):
     np.testing.assert_allclose(dq, g["dq"][0][rows], atol=1e-14)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_rowset_parts_sum_to_whole_head(causal):
+    """Splitting the query rows into sets and adding their dK/dV parts gives
+    the whole-head dK/dV; dQ rows match."""
+    N, d, scale = 24, 5, 0.4
+    q, k, v, dout = (_rand((N, d), s) for s in (95, 96, 97, 98))
+    g = oracle.attn_bwd(q[None], k[None], v[None], dout[None], scale, causal)
+    dk = np.zeros((N, d)); dv = np.zeros((N, d))
+    for rows in (list(range(0, N, 3)), list(range(1, N, 3)), list(range(2, N, 3))):
+        dq_r, dk_p, dv_p = oracle.attn_bwd_rowset(q, k, v, dout, rows, scale, causal)
+        np.testing.assert_allclose(dq_r, g["dq"][0][rows], atol=1e-14)
+        dk += dk_p; dv += dv_p
+    np.testing.assert_allclose(dk, g["dk"][0], atol=1e-13)
+    np.testing.assert_allclose(dv, g["dv"][0], atol=1e-13)
+
+
 def test_rejects_bad_rows():
     q = np.zeros((4, 2))
     with pytest.raises(RuntimeError):
