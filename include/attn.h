@@ -114,6 +114,41 @@ ATTN_API attn_status_t attn_bwd_stage(int stage, const void *q, const void *k, c
                              void *dv, void *workspace, size_t workspace_bytes, int B, int H, int N,
                              int d, float scale, int causal, attn_dtype_t dtype, void *stream);
 
+/*
+ * Size of the fixed scratch array that attn_bwd_noalloc uses (64 MiB).
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * Backward pass for callers that cannot allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for callers that own all
+ * device memory themselves and forbid allocations by the code they call (a
+ * serving engine with one pool sized at start-up, a plugin host that hands out
+ * only inputs and outputs), or that cannot accept cudaMalloc's implicit
+ * synchronisation or a late out-of-memory failure.
+ *
+ * Same computation and arguments as attn_bwd_ex, minus the workspace: the
+ * scratch it needs (attn_bwd_workspace_size(B, H, N, d) bytes) comes from one
+ * fixed device array of ATTN_NOALLOC_SCRATCH_BYTES inside this library.  The
+ * driver reserves that array on each GPU when it loads the library's device
+ * code, and it stays reserved until the process exits.  No call allocates or
+ * frees memory.
+ *  - Sizes whose scratch exceeds ATTN_NOALLOC_SCRATCH_BYTES return
+ *    ATTN_ERR_WORKSPACE and queue nothing; other argument errors are those of
+ *    attn_bwd_ex.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current; make that first call
+ *    before any stream capture.
+ *  - Every call on a device shares the one array, which keeps the last call's
+ *    contents (the backward rewrites or zeroes all of it that it reads).
+ *    Calls whose work overlaps on the GPU (different streams without ordering
+ *    between them) race on the array: order them.
+ */
+ATTN_API attn_status_t attn_bwd_noalloc(const void *q, const void *k, const void *v,
+                               const void *o, const void *dout, const float *lse, void *dq,
+                               void *dk, void *dv, int B, int H, int N, int d, float scale,
+                               int causal, attn_dtype_t dtype, void *stream);
+
 /* Static string naming a status code. */
 ATTN_API const char *attn_status_string(attn_status_t status);
 
