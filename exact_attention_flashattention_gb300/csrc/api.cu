@@ -35,6 +35,7 @@ EncodeTiledFn encode_fn() {
 }
 
 struct DevInfo {
+    int device = 0;
     int sms = 0;
     int* err_ptr = nullptr;
 };
@@ -49,6 +50,7 @@ bool dev_info(DevInfo& out) {
     std::lock_guard<std::mutex> lk(mu);
     if (!have[dev]) {
         DevInfo di;
+        di.device = dev;
         if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         if (cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err_ptr), g_device_error) != cudaSuccess) return false;
         cache[dev] = di;
@@ -189,6 +191,7 @@ attn_status_t bwd_common(int stage, const void* q, const void* k, const void* v,
     a.causal = causal ? 1 : 0;
     a.fp16 = dtype == ATTN_FP16;
     a.num_sms = di.sms;
+    a.device = di.device;
     a.error = di.err_ptr;
     if (launch_bwd(a, static_cast<cudaStream_t>(stream), stage) != cudaSuccess) return ATTN_ERR_CUDA;
     t_last_launches = stage < 0 ? 3 : 1;
@@ -244,7 +247,7 @@ attn_status_t attn_last_device_error(void* stream) {
     if (v != 0) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-        return ATTN_ERR_TIMEOUT;
+        return v == kDevSmemAlign ? ATTN_ERR_CUDA : ATTN_ERR_TIMEOUT;
     }
     return ATTN_OK;
 }

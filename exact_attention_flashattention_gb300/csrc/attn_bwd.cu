@@ -30,7 +30,9 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPanelBytes = 128 * 128;
 
 // ---------------------------------------------------------------- preprocess
-// D_r = sum_c dO[r,c] O[r,c] (FP32), lse2_r = L_r log2(e), dq_acc[r,:] = 0.
+// ndelta_r = -sum_c dO[r,c] O[r,c] (FP32, the negated D of the backward
+// equations), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.  The main kernel adds
+// the negated values inside packed FP32 pairs.
 // A group of D/8 threads handles one row; each thread reads 16 bytes of O and dO.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
@@ -67,8 +69,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
         dq_acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
         dq_acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (part == 0) {
-            delta[row] = acc;
-            lse2[row] = lse[row] * kLog2e;
+            delta[row] = -acc;
+            lse2[row] = -lse[row] * kLog2e;
         }
     }
 }
@@ -85,6 +87,9 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restric
 }
 
 // ---------------------------------------------------------------- main kernel
+// Shared memory: K_j, V_j (one tile each), Q_i and dO_i (two stages each), dS
+// (128 x 128 16-bit, written by the elementwise warps as the MN-major A operand
+// of dQ = dS K_j), and per stage the 128 values of -L log2(e) and of -D.
 template <int D>
 struct BwdLayout {
     static constexpr int kTile = 128 * D * 2;
@@ -93,66 +98,83 @@ struct BwdLayout {
     static constexpr int kV = kTile;
     static constexpr int kQ = 2 * kTile;          // [2 stages]
     static constexpr int kDO = 4 * kTile;         // [2 stages]
-    static constexpr int kDS = 6 * kTile;         // dS^T, 128 x 128 16-bit, 2 panels
-    static constexpr int kAux = kDS + 2 * kPanelBytes;
-    static constexpr int kBarKVFull = 0, kBarKVEmpty = 1;
-    static constexpr int kBarQFull = 2;    // [2]
-    static constexpr int kBarQEmpty = 4;   // [2]
-    static constexpr int kBarSdpFull = 6, kBarDsReady = 7, kBarDsFree = 8;
-    static constexpr int kBarDqFull = 9, kBarDqFree = 10, kBarDkvFull = 11, kBarDkvEmpty = 12;
-    static constexpr int kBarTeardown = 13;
-    static constexpr int kNumBars = 14;
+    static constexpr int kDS = 6 * kTile;         // 2 panels of 128 rows x 128 bytes
+    static constexpr int kVec = kDS + 2 * kPanelBytes;  // [2 stages][-L log2 e (128) | -D (128)] FP32
+    static constexpr int kAux = kVec + 2 * 256 * 4;
+    static constexpr int kBarKFull = 0, kBarKEmpty = 1, kBarVFull = 2, kBarVEmpty = 3;
+    static constexpr int kBarQFull = 4;    // [2]: Q_i, dO_i and the two vectors of stage i % 2
+    static constexpr int kBarQEmpty = 6;   // [2]
+    static constexpr int kBarSFull = 8, kBarDpFull = 9, kBarPReady = 10, kBarDsReady = 11;
+    static constexpr int kBarDqFull = 12, kBarDqFree = 13, kBarDkvFull = 14, kBarDkvEmpty = 15;
+    static constexpr int kBarTeardown = 16;
+    static constexpr int kNumBars = 17;
     static constexpr int kMiscOff = kAux + kNumBars * 8;
     static constexpr int kBytes = kMiscOff + 16;
-    static constexpr int kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384, kTmemDQ = 256;
+    // TMEM columns: dV, dK accumulators; S^T (P^T packed over it); dP^T (dS^T packed over it),
+    // reused for the dQ_i tile once dK has consumed dS^T.
+    static constexpr int kTmemDV = 0, kTmemDK = 128, kTmemS = 256, kTmemDP = 384, kTmemDQ = 384;
 };
 
 struct BwdItem {
     int bh, j, i0, n;   // head, key/value tile, first query tile, number of query tiles
 };
-__device__ __forceinline__ BwdItem decode_bwd(int idx, int T, int causal) {
-    BwdItem w;
-    w.bh = idx / T;
-    w.j = idx % T;     // within a head, j = 0 (the longest under the causal mask) first
+
+// Work list.  Causal: units of two key/value tiles of one head, j and T-1-j, longest first.
+// Tile j meets T-j query tiles, so every unit holds T+1 of them and a static round-robin of
+// units over the persistent CTAs is balanced.  Non-causal: one tile per unit (all equally
+// long; a finer grain shortens the tail).  Consecutive units share a head, so the CTAs
+// running at one time reuse that head's Q / dO from L2.
+__device__ __forceinline__ int bwd_units_per_head(int T, int causal) { return causal ? (T + 1) / 2 : T; }
+
+__device__ __forceinline__ bool bwd_item(int u, int s, int T, int causal, BwdItem& w) {
+    const int uph = bwd_units_per_head(T, causal);
+    const int jp = u % uph;
+    if (causal) {
+        const int jl = T - 1 - jp;
+        if (s == 1 && jl == jp) return false;
+        w.j = s ? jl : jp;
+    } else {
+        if (s == 1) return false;
+        w.j = jp;
+    }
+    w.bh = u / uph;
     w.i0 = causal ? w.j : 0;
     w.n = T - w.i0;
-    return w;
+    return true;
 }
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                const float* __restrict__ lse2, const float* __restrict__ delta, float* __restrict__ dq_acc,
+                const float* __restrict__ nlse2, const float* __restrict__ ndelta, float* __restrict__ dq_acc,
                 void* __restrict__ dk_out, void* __restrict__ dv_out, int BH, int N, float scale, int causal,
-                int* error) {
+                int smem_slack, int* error) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+    if ((int)pad > smem_slack) {
+        // The tiles need 1024-byte alignment and the launch could not give this much slack.
+        if (threadIdx.x == 0) atomicCAS(error, 0, kDevSmemAlign);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kAux);
+    const float* vec = reinterpret_cast<const float*>(smem + L::kVec);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int T = N / 128;
-    const int n_items = BH * T;
+    const int n_units = BH * bwd_units_per_head(T, causal);
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[L::kBarKVFull], 1);
-        mbar_init(&bars[L::kBarKVEmpty], 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars[L::kBarQFull + s], 1);
-            mbar_init(&bars[L::kBarQEmpty + s], 1);
-        }
-        mbar_init(&bars[L::kBarSdpFull], 1);
+        for (int b = 0; b < L::kNumBars; ++b) mbar_init(&bars[b], 1);
+        mbar_init(&bars[L::kBarPReady], 256);
         mbar_init(&bars[L::kBarDsReady], 256);
-        mbar_init(&bars[L::kBarDsFree], 1);
-        mbar_init(&bars[L::kBarDqFull], 1);
         mbar_init(&bars[L::kBarDqFree], 128);
-        mbar_init(&bars[L::kBarDkvFull], 1);
         mbar_init(&bars[L::kBarDkvEmpty], 128);
-        mbar_init(&bars[L::kBarTeardown], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -174,127 +196,156 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const float scale_log2 = scale * kLog2e;
 
     if (warp < 8) {
-        regs_inc<144>();
         // ------------------------------------------------------ P and dS (elementwise)
-        const int half = warp >> 2;
+        regs_inc<144>();
+        const int half = warp >> 2;              // query columns [64 half, 64 half + 64)
         const int row = (warp & 3) * 32 + lane;  // key row within the tile (TMEM lane)
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t s_addr = tmem + lane_base + L::kTmemS + 64 * half;
         const uint32_t dp_addr = tmem + lane_base + L::kTmemDP + 64 * half;
         uint8_t* ds_panel = smem + L::kDS + half * kPanelBytes;
+        const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
         uint32_t g = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-            const BwdItem w = decode_bwd(idx, T, causal);
-            for (int it = 0; it < w.n; ++it, ++g) {
-                const int i = w.i0 + it;
-                const bool diag = causal && i == w.j;
-                if (!mbar_wait(&bars[L::kBarSdpFull], g & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
-                if (!mbar_wait(&bars[L::kBarDsFree], (g & 1) ^ 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
-                tc_fence_after();
-                const float* l2row = lse2 + (size_t)w.bh * N + (size_t)i * 128 + 64 * half;
-                const float* drow = delta + (size_t)w.bh * N + (size_t)i * 128 + 64 * half;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int sidx = 0; sidx < 2 && ok; ++sidx) {
+                BwdItem w;
+                if (!bwd_item(u, sidx, T, causal, w)) break;
+                for (int it = 0; it < w.n; ++it, ++g) {
+                    const int i = w.i0 + it;
+                    const bool diag = causal && i == w.j;
+                    const float2* nl = reinterpret_cast<const float2*>(vec + (g & 1) * 256 + 64 * half);
+                    const float2* nd = reinterpret_cast<const float2*>(vec + (g & 1) * 256 + 128 + 64 * half);
+                    // P^T = 2^(S^T scale log2 e - L log2 e), keys > queries masked on the diagonal tile
+                    if (!mbar_wait(&bars[L::kBarSFull], g & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                    tc_fence_after();
+                    float p[64];
+                    {
+                        uint32_t s[64];
+                        tmem_ld32(s_addr, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+                        tmem_ld32(s_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+                        tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t s[32], dp[32];
-                    tmem_ld32(s_addr + 32 * c, s);
-                    tmem_ld32(dp_addr + 32 * c, dp);
-                    float lv[32], dv[32];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float4 a = __ldg(reinterpret_cast<const float4*>(l2row + 32 * c) + e);
-                        const float4 b = __ldg(reinterpret_cast<const float4*>(drow + 32 * c) + e);
-                        lv[4 * e] = a.x; lv[4 * e + 1] = a.y; lv[4 * e + 2] = a.z; lv[4 * e + 3] = a.w;
-                        dv[4 * e] = b.x; dv[4 * e + 1] = b.y; dv[4 * e + 2] = b.z; dv[4 * e + 3] = b.w;
-                    }
-                    tmem_wait_ld();
-                    uint32_t pk[16], dk16[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int q0 = 64 * half + 32 * c + 2 * e;  // query column within the tile
-                        float p0 = ex2_ftz(fmaf(__uint_as_float(s[2 * e]), scale_log2, -lv[2 * e]));
-                        float p1 = ex2_ftz(fmaf(__uint_as_float(s[2 * e + 1]), scale_log2, -lv[2 * e + 1]));
-                        if (diag) {
-                            // key row > query column is masked (P = dS = 0)
-                            if (row > q0) p0 = 0.f;
-                            if (row > q0 + 1) p1 = 0.f;
+                        for (int e = 0; e < 32; ++e) {
+                            const float2 l = nl[e];
+                            const uint64_t x = f2_fma(f2_pack(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                                                      sl2, f2_pack(l.x, l.y));
+                            float x0, x1;
+                            f2_unpack(x, x0, x1);
+                            p[2 * e] = ex2_ftz(x0);
+                            p[2 * e + 1] = ex2_ftz(x1);
                         }
-                        const float ds0 = p0 * (__uint_as_float(dp[2 * e]) - dv[2 * e]);
-                        const float ds1 = p1 * (__uint_as_float(dp[2 * e + 1]) - dv[2 * e + 1]);
-                        pk[e] = pack2<BF16>(p0, p1);
-                        dk16[e] = pack2<BF16>(ds0, ds1);
-                    }
-                    tmem_st16(s_addr + 16 * c, pk);
-                    tmem_st16(dp_addr + 16 * c, dk16);
-                    // dS^T row -> shared memory (128B-swizzled, MN-major A operand of dQ = dS K)
+                        if (diag) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        uint4* dst = reinterpret_cast<uint4*>(ds_panel + sw128_offset(row, 4 * c + e));
-                        *dst = make_uint4(dk16[4 * e], dk16[4 * e + 1], dk16[4 * e + 2], dk16[4 * e + 3]);
+                            for (int e = 0; e < 64; ++e)
+                                if (row > 64 * half + e) p[e] = 0.f;
+                        }
+#pragma unroll
+                        for (int c = 0; c < 2; ++c) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pk[e] = pack2<BF16>(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]);
+                            tmem_st16(s_addr + 16 * c, pk);
+                        }
                     }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars[L::kBarPReady]);
+
+                    // dS^T = P^T o (dP^T - D): into TMEM (A operand of dK) and shared memory (dQ)
+                    if (!mbar_wait(&bars[L::kBarDpFull], g & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                    if (!mbar_wait(&bars[L::kBarDqFull], (g & 1) ^ 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+                    tc_fence_after();
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t dp[32];
+                        tmem_ld32(dp_addr + 32 * c, dp);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 dl = nd[16 * c + e];
+                            const uint64_t t = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                                      f2_pack(dl.x, dl.y));
+                            const uint64_t ds = f2_mul(f2_pack(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]), t);
+                            float d0, d1;
+                            f2_unpack(ds, d0, d1);
+                            pk[e] = pack2<BF16>(d0, d1);
+                        }
+                        tmem_st16(dp_addr + 16 * c, pk);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            uint4* dst = reinterpret_cast<uint4*>(ds_panel + sw128_offset(row, 4 * c + e));
+                            *dst = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    tmem_wait_st();
+                    tc_fence_before();
+                    mbar_arrive(&bars[L::kBarDsReady]);
                 }
-                fence_proxy_async_smem();
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(&bars[L::kBarDsReady]);
             }
         }
     } else if (warp < 12) {
-        regs_dec<112>();
         // ------------------------------------------------------ dQ drain, dK/dV epilogue
+        regs_dec<112>();
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t g = 0;
         int k = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-            const BwdItem w = decode_bwd(idx, T, causal);
-            for (int it = 0; it < w.n; ++it, ++g) {
-                const int i = w.i0 + it;
-                if (!mbar_wait(&bars[L::kBarDqFull], g & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
-                tc_fence_after();
-                float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
+        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
+                BwdItem w;
+                if (!bwd_item(u, sidx, T, causal, w)) break;
+                for (int it = 0; it < w.n; ++it, ++g) {
+                    const int i = w.i0 + it;
+                    if (!mbar_wait(&bars[L::kBarDqFull], g & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                    tc_fence_after();
+                    float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t r[32];
-                    tmem_ld32(tmem + lane_base + L::kTmemDQ + 32 * c, r);
-                    tmem_wait_ld();
-                    if (c == D / 32 - 1) {
-                        tc_fence_before();
-                        mbar_arrive(&bars[L::kBarDqFree]);
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t r[64];
+                        tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                        tmem_wait_ld();
+                        if (h == D / 64 - 1) {
+                            tc_fence_before();
+                            mbar_arrive(&bars[L::kBarDqFree]);
+                        }
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            red_add_v4(dst + 64 * h + 4 * e, __uint_as_float(r[4 * e]) * scale,
+                                       __uint_as_float(r[4 * e + 1]) * scale, __uint_as_float(r[4 * e + 2]) * scale,
+                                       __uint_as_float(r[4 * e + 3]) * scale);
                     }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        red_add_v4(dst + 32 * c + 4 * e, __uint_as_float(r[4 * e]) * scale,
-                                   __uint_as_float(r[4 * e + 1]) * scale, __uint_as_float(r[4 * e + 2]) * scale,
-                                   __uint_as_float(r[4 * e + 3]) * scale);
                 }
-            }
-            if (!ok) break;
-            if (!mbar_wait(&bars[L::kBarDkvFull], k & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
-            tc_fence_after();
-            const size_t grow = (size_t)w.bh * N + (size_t)w.j * 128 + row;
+                if (!ok) break;
+                if (!mbar_wait(&bars[L::kBarDkvFull], k & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                tc_fence_after();
+                const size_t grow = (size_t)w.bh * N + (size_t)w.j * 128 + row;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t src = tmem + lane_base + (which ? L::kTmemDK : L::kTmemDV);
-                const float mul = which ? scale : 1.f;
-                uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow * D * 2;
+                for (int which = 0; which < 2; ++which) {
+                    const uint32_t src = tmem + lane_base + (which ? L::kTmemDK : L::kTmemDV);
+                    const float mul = which ? scale : 1.f;
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow * D * 2;
 #pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(src + c, r);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
+                    for (int c = 0; c < D; c += 32) {
+                        uint32_t r[32];
+                        tmem_ld32(src + c, r);
+                        tmem_wait_ld();
+                        uint32_t pk[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
-                    uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
+                        for (int e = 0; e < 16; ++e)
+                            pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
                 }
+                tc_fence_before();
+                mbar_arrive(&bars[L::kBarDkvEmpty]);
             }
-            tc_fence_before();
-            mbar_arrive(&bars[L::kBarDkvEmpty]);
         }
     } else {
         regs_dec<112>();  // warps 12-15; the split 2x144 + 112 + 112 warpgroups uses 65536 registers
@@ -309,58 +360,68 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-                const BwdItem w = decode_bwd(idx, T, causal);
-                if (!mbar_wait(&bars[L::kBarKVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                tc_fence_after();
-                for (int it = 0; it < w.n; ++it, ++g) {
-                    const uint32_t st = g & 1;
-                    if (!mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                    if (!mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
+                    BwdItem w;
+                    if (!bwd_item(u, sidx, T, causal, w)) break;
+                    if (!mbar_wait(&bars[L::kBarKFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    if (!mbar_wait(&bars[L::kBarVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
-                    // S^T = K_j Q_i^T and dP^T = V_j dO_i^T (both K-major operands)
+                    for (int it = 0; it < w.n; ++it, ++g) {
+                        const uint32_t st = g & 1;
+                        const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
+                        if (!mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        tc_fence_after();
+                        // S^T = K_j Q_i^T (its TMEM columns were last read by the previous dV, issued earlier)
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                        mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024),
-                               kIdescS, kk > 0);
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024),
+                                   sdesc_sw128(qs + off, 16, 1024), kIdescS, kk > 0);
+                        }
+                        mma_commit(&bars[L::kBarSFull]);
+                        // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
+                        if (!mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+                            mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024),
+                                   sdesc_sw128(dos + off, 16, 1024), kIdescS, kk > 0);
+                        }
+                        mma_commit(&bars[L::kBarDpFull]);
+                        if (it == w.n - 1) mma_commit(&bars[L::kBarVEmpty]);
+                        // dV += P^T dO_i
+                        if (!mbar_wait(&bars[L::kBarPReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (it == 0 && !mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+                            mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol,
+                                   sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        // dK += dS^T Q_i
+                        if (!mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        tc_fence_after();
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
+                            mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol,
+                                   sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&bars[L::kBarQEmpty + st]);
+                        // dQ_i = dS K_j (A = dS from shared memory, MN-major; B = K_j MN-major)
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(tmem + L::kTmemDQ, sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024),
+                                   sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024), kIdescQ, kk > 0);
+                        mma_commit(&bars[L::kBarDqFull]);
                     }
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                        mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024), sdesc_sw128(dos + off, 16, 1024),
-                               kIdescS, kk > 0);
-                    }
-                    mma_commit(&bars[L::kBarSdpFull]);
-                    if (!mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                    if (it == 0 && !mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                    tc_fence_after();
-                    // dV += P^T dO_i ; dK += dS^T Q_i  (A from TMEM, B = dO_i / Q_i MN-major)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                        mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol, sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024),
-                               kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                        mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol, sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024),
-                               kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
-                    }
-                    mma_commit(&bars[L::kBarQEmpty + st]);
-                    // dQ_i = dS K_j (A = dS from shared memory, MN-major; B = K_j MN-major)
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + L::kTmemDQ, sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024),
-                               sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024), kIdescQ, kk > 0);
-                    mma_commit(&bars[L::kBarDqFull]);
-                    mma_commit(&bars[L::kBarDsFree]);
+                    if (!ok) break;
+                    mma_commit(&bars[L::kBarKEmpty]);
+                    mma_commit(&bars[L::kBarDkvFull]);
                 }
-                if (!ok) break;
-                mma_commit(&bars[L::kBarDkvFull]);
-                mma_commit(&bars[L::kBarKVEmpty]);
             }
             mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
@@ -369,33 +430,52 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
-            int issued_kv = -1;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-                const BwdItem w = decode_bwd(idx, T, causal);
-                if (!mbar_wait(&bars[L::kBarKVEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
-                mbar_arrive_expect_tx(&bars[L::kBarKVFull], 2 * L::kTile);
-                issued_kv = k;
+            int last_kv = -1;
+            auto load_q = [&](const BwdItem& w, int it) -> bool {
+                const int i = w.i0 + it;
+                const uint32_t st = g & 1;
+                if (!mbar_wait(&bars[L::kBarQEmpty + st], ((g >> 1) & 1) ^ 1, guard, kDevTimeoutLoad)) return false;
+                mbar_arrive_expect_tx(&bars[L::kBarQFull + st], 2 * L::kTile + 1024);
 #pragma unroll
                 for (int p = 0; p < L::kPanels; ++p) {
-                    tma_load_3d(smem + L::kK + p * kPanelBytes, &tm_k, &bars[L::kBarKVFull], 64 * p, w.j * 128, w.bh);
-                    tma_load_3d(smem + L::kV + p * kPanelBytes, &tm_v, &bars[L::kBarKVFull], 64 * p, w.j * 128, w.bh);
+                    tma_load_3d(smem + L::kQ + st * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + st],
+                                64 * p, i * 128, w.bh);
+                    tma_load_3d(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
+                                64 * p, i * 128, w.bh);
                 }
-                for (int it = 0; it < w.n; ++it, ++g) {
-                    const int i = w.i0 + it;
-                    const uint32_t st = g & 1;
-                    if (!mbar_wait(&bars[L::kBarQEmpty + st], ((g >> 1) & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
-                    mbar_arrive_expect_tx(&bars[L::kBarQFull + st], 2 * L::kTile);
+                const size_t r0 = (size_t)w.bh * N + (size_t)i * 128;
+                bulk_load(smem + L::kVec + st * 1024, nlse2 + r0, 512, &bars[L::kBarQFull + st]);
+                bulk_load(smem + L::kVec + st * 1024 + 512, ndelta + r0, 512, &bars[L::kBarQFull + st]);
+                ++g;
+                return true;
+            };
+            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+                for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
+                    BwdItem w;
+                    if (!bwd_item(u, sidx, T, causal, w)) break;
+                    // V_j as soon as the previous item's last dP^T is done, then the first Q_i / dO_i,
+                    // then K_j once the previous item's last dQ is done, then the rest.
+                    if (!mbar_wait(&bars[L::kBarVEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bars[L::kBarVFull], L::kTile);
 #pragma unroll
-                    for (int p = 0; p < L::kPanels; ++p) {
-                        tma_load_3d(smem + L::kQ + st * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + st],
-                                    64 * p, i * 128, w.bh);
-                        tma_load_3d(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
-                                    64 * p, i * 128, w.bh);
-                    }
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_3d(smem + L::kV + p * kPanelBytes, &tm_v, &bars[L::kBarVFull], 64 * p, w.j * 128, w.bh);
+                    if (!load_q(w, 0)) { ok = false; break; }
+                    if (!mbar_wait(&bars[L::kBarKEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
+                    mbar_arrive_expect_tx(&bars[L::kBarKFull], L::kTile);
+                    last_kv = k;
+#pragma unroll
+                    for (int p = 0; p < L::kPanels; ++p)
+                        tma_load_3d(smem + L::kK + p * kPanelBytes, &tm_k, &bars[L::kBarKFull], 64 * p, w.j * 128, w.bh);
+                    for (int it = 1; it < w.n && ok; ++it)
+                        if (!load_q(w, it)) ok = false;
                 }
             }
             // Let every copy issued above land before shared memory is released.
-            if (issued_kv >= 0) mbar_wait_drain(&bars[L::kBarKVFull], issued_kv & 1, kWaitLimitNs);
+            if (last_kv >= 0) {
+                mbar_wait_drain(&bars[L::kBarKFull], last_kv & 1, kWaitLimitNs);
+                mbar_wait_drain(&bars[L::kBarVFull], last_kv & 1, kWaitLimitNs);
+            }
             for (uint32_t t = (g > 2 ? g - 2 : 0); t < g; ++t)
                 mbar_wait_drain(&bars[L::kBarQFull + (t & 1)], (t >> 1) & 1, kWaitLimitNs);
         }
@@ -427,15 +507,21 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     }
     // 2. main kernel
     if (stage < 0 || stage == 1) {
-        const int smem_bytes = L::kBytes + 1024;
+        int max_smem = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, a.device);
+        if (e != cudaSuccess) return e;
+        const int want = L::kBytes + 1024;
+        const int smem_bytes = want < max_smem ? want : max_smem;
+        const int slack = smem_bytes - L::kBytes;
+        if (slack < 0) return cudaErrorInvalidConfiguration;
         auto kern = attn_bwd_kernel<D, BF16>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
         const int T = a.N / 128;
-        const long n_items = (long)a.BH * T;
-        const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
-        kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc, a.dk,
-                                                      a.dv, a.BH, a.N, a.scale, a.causal, a.error);
+        const long n_units = (long)a.BH * (a.causal ? (T + 1) / 2 : T);
+        const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
+        kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
+                                                      a.dk, a.dv, a.BH, a.N, a.scale, a.causal, slack, a.error);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

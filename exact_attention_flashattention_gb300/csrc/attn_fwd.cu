@@ -58,8 +58,7 @@ struct FwdLayout {
     static constexpr int kScaleOff = kAux + 8 * 64;                // float [2][128]
     static constexpr int kFinLOff = kScaleOff + 2 * 128 * 4;       // float [2 buf][2 q][128]
     static constexpr int kFinMOff = kFinLOff + 4 * 128 * 4;        // float [2 buf][2 q][128]
-    static constexpr int kFinLqOff = kFinMOff + 4 * 128 * 4;       // float [2 buf][2 q][128]
-    static constexpr int kMiscOff = kFinLqOff + 4 * 128 * 4;       // tmem base, abort flag
+    static constexpr int kMiscOff = kFinMOff + 4 * 128 * 4;        // tmem base, abort flag
     static constexpr int kBytes = kMiscOff + 64;
     static constexpr int kTmemS = 0;     // S_q at kTmemS + 128 q
     static constexpr int kTmemO = 256;   // O_q at kTmemO + 128 q
@@ -72,16 +71,48 @@ struct WorkItem {
     int n0, n1;       // number of KV tiles for each Q tile
 };
 
-__device__ __forceinline__ WorkItem decode_item(int idx, int M, int T, int causal) {
-    WorkItem w;
-    w.bh = idx / M;
-    w.m = M - 1 - (idx % M);  // within a head, longest Q tile pair first
-    w.t0 = 2 * w.m;
-    w.t1 = 2 * w.m + 1;
+// Work list.  Causal: units of two Q tile pairs of one head, m and M-1-m, longest first.  The
+// pair m meets 2m+1 and 2m+2 key/value tiles, so every unit holds the same amount of work and
+// a static round-robin of units over the persistent CTAs is balanced.  Non-causal: every item
+// is equally long, so each unit is one item (a finer grain shortens the tail).  Consecutive
+// units share a head, so the CTAs running at one time reuse its K / V from L2.
+__device__ __forceinline__ int fwd_units_per_head(int M, int causal) { return causal ? (M + 1) / 2 : M; }
+
+__device__ __forceinline__ bool fwd_item(int u, int s, int M, int T, int causal, WorkItem& w) {
+    const int uph = fwd_units_per_head(M, causal);
+    const int mp = u % uph;
+    int m;
+    if (causal) {
+        const int ml = M - 1 - mp;
+        if (s == 1 && ml == mp) return false;
+        m = s ? mp : ml;
+    } else {
+        if (s == 1) return false;
+        m = M - 1 - mp;
+    }
+    w.bh = u / uph;
+    w.m = m;
+    w.t0 = 2 * m;
+    w.t1 = 2 * m + 1;
     w.n0 = causal ? min(w.t0 + 1, T) : T;
     w.n1 = causal ? min(w.t1 + 1, T) : T;
-    return w;
+    return true;
 }
+
+// This CTA's sequence of work items: units blockIdx.x, blockIdx.x + gridDim.x, ...
+// (position kept as 2 * unit + slot in one register).
+struct FwdIter {
+    int pos;
+    __device__ FwdIter() : pos(2 * (int)blockIdx.x) {}
+    __device__ bool next(WorkItem& w, int M, int T, int causal, int n_units) {
+        for (;;) {
+            const int u = pos >> 1, s = pos & 1;
+            if (u >= n_units) return false;
+            pos = s ? 2 * (u + (int)gridDim.x) : pos + 1;
+            if (fwd_item(u, s, M, T, causal, w)) return true;
+        }
+    }
+};
 
 template <int D, bool BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -96,7 +127,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     float* scale_buf = reinterpret_cast<float*>(smem + L::kScaleOff);
     float* fin_l = reinterpret_cast<float*>(smem + L::kFinLOff);
     float* fin_m = reinterpret_cast<float*>(smem + L::kFinMOff);
-    float* fin_lq = reinterpret_cast<float*>(smem + L::kFinLqOff);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     int* abort_flag = reinterpret_cast<int*>(smem + L::kMiscOff + 4);
 
@@ -104,7 +134,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int lane = threadIdx.x & 31;
     const int T = N / 128;
     const int M = (T + 1) / 2;
-    const int n_items = BH * M;
+    const int n_units = BH * fwd_units_per_head(M, causal);
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::kBarQFull], 1);
@@ -152,12 +182,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t s_phase = 0;
         int k = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-            const WorkItem w = decode_item(idx, M, T, causal);
+        WorkItem w;
+        for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
             const int t = q ? w.t1 : w.t0;
             const int n = q ? w.n1 : w.n0;
             const int diag = (causal && t < T) ? t : -1;
-            float m_run = -INFINITY, l_run = 0.f, lq_run = 0.f;
+            float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < n; ++j) {
                 if (!mbar_wait(&bars[L::kBarSFull + q], s_phase, guard, kDevTimeoutSoftmax)) { ok = false; break; }
                 s_phase ^= 1;
@@ -189,18 +219,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 } else if (tile_max - m_run > kRescaleThreshold) {
                     alpha = ex2_ftz(m_run - tile_max);
                     l_run *= alpha;
-                    lq_run *= alpha;
                     m_run = tile_max;
                 }
                 scale_buf[q * 128 + row] = alpha;
                 mbar_arrive(&bars[L::kBarStats + q]);
 
-                // p = 2^(s * scale * log2(e) - m), rounded to 16 bits for the PV MMA.  Two row
-                // sums: l (exact p) gives L, lq (the rounded p the MMA actually uses) normalises
-                // O = (P V) / lq, so a dominant weight's rounding cancels in O.
+                // p = 2^(s * scale * log2(e) - m), rounded to 16 bits for the PV MMA; the row sum
+                // l adds the FP32 values (it gives L and normalises O).
                 const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
                 const uint64_t nm2 = f2_pack(-m_run, -m_run);
-                uint64_t acc = 0, accq = 0;
+                uint64_t acc0 = 0, acc1 = 0;
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     uint32_t pk[16];
@@ -212,20 +240,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         f2_unpack(x, x0, x1);
                         const float p0 = ex2_ftz(x0), p1 = ex2_ftz(x1);
                         pk[c] = pack2<BF16>(p0, p1);
-                        acc = f2_add(acc, f2_pack(p0, p1));
-                        accq = f2_add(accq, unpack2<BF16>(pk[c]));
+                        if (c & 1) acc1 = f2_add(acc1, f2_pack(p0, p1));
+                        else acc0 = f2_add(acc0, f2_pack(p0, p1));
                     }
                     tmem_st16(s_addr + 16 * h, pk);
                 }
-                float sum0, sum1, sq0, sq1;
-                f2_unpack(acc, sum0, sum1);
-                f2_unpack(accq, sq0, sq1);
-                l_run += sum0 + sum1;
-                lq_run += sq0 + sq1;
+                float sa, sb, sc, sd;
+                f2_unpack(acc0, sa, sb);
+                f2_unpack(acc1, sc, sd);
+                l_run += (sa + sb) + (sc + sd);
                 if (j == n - 1) {
                     const int b = k & 1;
                     fin_l[(b * 2 + q) * 128 + row] = l_run;
-                    fin_lq[(b * 2 + q) * 128 + row] = lq_run;
                     fin_m[(b * 2 + q) * 128 + row] = m_run;
                     mbar_arrive(&bars[L::kBarFin + 2 * q + b]);
                 }
@@ -242,8 +268,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t stats_phase[2] = {0, 0}, o_phase[2] = {0, 0};
         int k = 0;
         bool ok = true;
-        for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-            const WorkItem w = decode_item(idx, M, T, causal);
+        WorkItem w;
+        for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
             for (int j = 0; j < w.n1 && ok; ++j) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -283,11 +309,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!mbar_wait(&bars[L::kBarFin + 2 * q + b], (k >> 1) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
                 tc_fence_after();
                 const float l = fin_l[(b * 2 + q) * 128 + row];
-                const float lq = fin_lq[(b * 2 + q) * 128 + row];
                 const float mrow = fin_m[(b * 2 + q) * 128 + row];
                 const int t = q ? w.t1 : w.t0;
                 const int grow = t * 128 + row;
-                const float inv_l = 1.f / lq;
+                const float inv_l = 1.f / l;
                 const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
                 uint8_t* dst = reinterpret_cast<uint8_t*>(o_out) + ((size_t)w.bh * N + grow) * (size_t)D * 2;
 #pragma unroll 1
@@ -346,8 +371,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after();
                 return r;
             };
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x) {
-                const WorkItem w = decode_item(idx, M, T, causal);
+            WorkItem w;
+            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units);) {
                 if (!mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
                 q_phase ^= 1;
                 tc_fence_after();
@@ -395,8 +420,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             int k = 0;
             bool ok = true;
             int last_q_item = -1;
-            for (int idx = blockIdx.x; idx < n_items && ok; idx += gridDim.x, ++k) {
-                const WorkItem w = decode_item(idx, M, T, causal);
+            WorkItem w;
+            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
                 if (k > 0 && !mbar_wait(&bars[L::kBarQEmpty], (k - 1) & 1, guard, kDevTimeoutLoad)) { ok = false; break; }
                 mbar_arrive_expect_tx(&bars[L::kBarQFull], 2 * L::kTile);
                 last_q_item = k;
@@ -448,8 +473,8 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     const int T = a.N / 128;
     const int M = (T + 1) / 2;
-    const long n_items = (long)a.BH * M;
-    const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
+    const long n_units = (long)a.BH * (a.causal ? (M + 1) / 2 : M);
+    const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
     if (grid <= 0) return cudaSuccess;
     kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.BH, a.N, a.scale,
                                                   a.causal, a.error);

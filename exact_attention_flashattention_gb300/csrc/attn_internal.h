@@ -15,6 +15,7 @@ enum DeviceError : int {
     kDevTimeoutMma = 2,      // the MMA issuer's wait gave up
     kDevTimeoutSoftmax = 3,  // a softmax / elementwise warp's wait gave up
     kDevTimeoutCorr = 4,     // a correction / epilogue warp's wait gave up
+    kDevSmemAlign = 5,       // dynamic shared memory could not be 1024-byte aligned (kernel did nothing)
 };
 
 // Wait limit for every mbarrier wait in the kernels (nanoseconds of
@@ -41,14 +42,15 @@ struct BwdArgs {
     void* dq;         // [BH, N, d]
     void* dk;
     void* dv;
-    float* delta;     // workspace [BH, N]   D = rowsum(dO o O)
-    float* lse2;      // workspace [BH, N]   L * log2(e)
+    float* delta;     // workspace [BH, N]   -D = -rowsum(dO o O)
+    float* lse2;      // workspace [BH, N]   -L * log2(e)
     float* dq_acc;    // workspace [BH, N, d] FP32
     int BH, N, d;
     float scale;
     int causal;
     int fp16;
     int num_sms;
+    int device;
     int* error;
 };
 

@@ -263,22 +263,16 @@ __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
-// The two values a packed 16-bit pair actually holds, as an FP32 pair.
-template <bool BF16>
-__device__ __forceinline__ uint64_t unpack2(uint32_t pk) {
-    if constexpr (BF16) {
-        return f2_pack(__uint_as_float(pk << 16), __uint_as_float(pk & 0xffff0000u));
-    } else {
-        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&pk));
-        return f2_pack(f.x, f.y);
-    }
-}
-
 // Register-count hand-off between warpgroups (must be executed by all warps
 // of a warpgroup).
 template <int N> __device__ __forceinline__ void regs_inc() {

@@ -155,7 +155,8 @@ ATTN_API const char *attn_status_string(attn_status_t status);
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel wait gave up;
- * its outputs are incomplete) or ATTN_ERR_CUDA (the synchronisation failed).
+ * its outputs are incomplete) or ATTN_ERR_CUDA (the synchronisation failed, or
+ * a kernel could not align its shared memory and wrote nothing).
  */
 ATTN_API attn_status_t attn_last_device_error(void *stream);
 

@@ -1,0 +1,135 @@
+"""CUDA path vs the FP64 oracle at the full sizes of the workload list, in the
+launch configuration bench.py times (persistent grid over every head).
+
+Whole heads are too slow for the oracle at these sizes, so it checks outputs it
+can compute one by one:
+  * O, L and dQ of sampled query rows (first and last rows, tile edges, random
+    rows) of sampled heads -- each needs one row of S, P, dP, dS;
+  * dK and dV of the last key tile under the causal mask, which only the last
+    128 query rows reach, so the oracle's sum over those rows is complete;
+  * for non-causal heads, dK and dV of one whole head (oracle rows split over
+    threads and summed);
+and, on every head, properties that hold at any size: no NaN / unwritten
+element, and sum_j dK_j = 0 (rows of dS sum to zero).
+"""
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from attn_cases import TOL_GRAD_RELFRO, TOL_L_MAXABS, o_tolerance, rel_fro, to_device, to_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CONFIGS = [
+    # id, B, H, N, d, causal, dtype, sigma_qk
+    ("causal_b8h16n4096d128", 8, 16, 4096, 128, True, "bf16", 1.0),
+    ("noncausal_b4h16n4096d128", 4, 16, 4096, 128, False, "bf16", 1.0),
+    ("noncausal_b2h16n8192d128", 2, 16, 8192, 128, False, "bf16", 1.0),
+    ("noncausal_b1h16n16384d128", 1, 16, 16384, 128, False, "bf16", 1.0),
+    ("fp16_causal_b4h16n1024d64", 4, 16, 1024, 64, True, "fp16", 1.0),
+    ("fp16_causal_b4h16n2048d64", 4, 16, 2048, 64, True, "fp16", 1.0),
+    ("fp16_causal_b4h16n4096d64", 4, 16, 4096, 64, True, "fp16", 1.0),
+    ("stress_b1h32n32768d128", 1, 32, 32768, 128, True, "bf16", 2.0),
+]
+SEED = 20261202
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import exact_attention_flashattention_gb300 as a
+    a.load()
+    return a
+
+
+def _sample_heads(BH):
+    rng = np.random.default_rng(BH)
+    extra = [int(x) for x in rng.choice(BH, size=min(2, BH), replace=False)]
+    return sorted(set([0, BH - 1] + extra))
+
+
+def _sample_rows(N, rng):
+    rows = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1}
+    rows.update(int(x) for x in rng.integers(0, N, size=22))
+    return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
+
+
+def _whole_head_dkdv(q, k, v, do, scale, causal, threads):
+    """dK, dV of one head from the oracle's row-set entry point, rows split over threads."""
+    N = q.shape[0]
+    chunks = np.array_split(np.arange(N, dtype=np.int64), threads)
+
+    def one(rows):
+        _, dk, dv = oracle.attn_bwd_rowset(q, k, v, do, rows, scale, causal)
+        return dk, dv
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(one, chunks))
+    return sum(p[0] for p in parts), sum(p[1] for p in parts)
+
+
+@pytest.mark.parametrize("cid,B,H,N,d,causal,dtype,sigma", CONFIGS, ids=[c[0] for c in CONFIGS])
+def test_full_size_against_oracle(attn, cid, B, H, N, d, causal, dtype, sigma):
+    BH = B * H
+    scale = 1.0 / math.sqrt(d)
+    threads = min(16, os.cpu_count() or 1)
+    bits = {n: si.tensor_heads(SEED, n, BH, N, d, sigma if n in ("q", "k") else 1.0, dtype, threads=threads)
+            for n in ("q", "k", "v", "do")}
+    q, k, v, do = (to_device(bits[n], B, H, dtype) for n in ("q", "k", "v", "do"))
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    attn.attn_fwd(q, k, v, o, lse, scale, causal)
+    attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, scale, causal)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+
+    # properties on every head
+    for name, t in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert bool(torch.isfinite(t).all()), f"{name}: unwritten or non-finite elements"
+    dkf = dk.float()
+    colsum = dkf.sum(dim=2).abs()
+    colabs = dkf.abs().sum(dim=2) + 1e-6
+    assert float((colsum / colabs).max()) < 2e-2, "sum_j dK_j != 0"
+
+    rng = np.random.default_rng(N + d)
+    worst = {"o": 0.0, "l": 0.0, "dq": 0.0, "dkdv_tail": 0.0}
+    og, lg, dqg = to_f64(o).reshape(BH, N, d), to_f64(lse).reshape(BH, N), to_f64(dq).reshape(BH, N, d)
+    for h in _sample_heads(BH):
+        x = {n: si.bits_to_f32(bits[n][h], dtype).astype(np.float64) for n in bits}
+        rows = _sample_rows(N, rng)
+        o_r, l_r, dq_r = oracle.attn_rows(x["q"], x["k"], x["v"], rows, scale, causal, dout=x["do"])
+        err = np.abs(og[h][rows] - o_r)
+        assert np.all(err <= o_tolerance(o_r, dtype)), (h, float(err.max()))
+        worst["o"] = max(worst["o"], float(err.max()))
+        le = float(np.max(np.abs(lg[h][rows] - l_r)))
+        assert le <= TOL_L_MAXABS, (h, le)
+        worst["l"] = max(worst["l"], le)
+        e = rel_fro(dqg[h][rows], dq_r)
+        assert e <= TOL_GRAD_RELFRO, (h, "dq rows", e)
+        worst["dq"] = max(worst["dq"], e)
+    # dK, dV checked exactly where the oracle can afford them
+    dkg, dvg = to_f64(dk).reshape(BH, N, d), to_f64(dv).reshape(BH, N, d)
+    h = BH - 1
+    x = {n: si.bits_to_f32(bits[n][h], dtype).astype(np.float64) for n in bits}
+    if causal:
+        tail = np.arange(N - 128, N, dtype=np.int64)
+        dq_t, dk_t, dv_t = oracle.attn_bwd_rowset(x["q"], x["k"], x["v"], x["do"], tail, scale, causal)
+        for name, got, ref in (("dq", dqg[h][tail], dq_t), ("dk", dkg[h][tail], dk_t[tail]),
+                               ("dv", dvg[h][tail], dv_t[tail])):
+            e = rel_fro(got, ref)
+            assert e <= TOL_GRAD_RELFRO, (name, "last tile", e)
+            worst["dkdv_tail"] = max(worst["dkdv_tail"], e)
+    elif N <= 8192:
+        dk_r, dv_r = _whole_head_dkdv(x["q"], x["k"], x["v"], x["do"], scale, causal, threads)
+        for name, got, ref in (("dk", dkg[h], dk_r), ("dv", dvg[h], dv_r)):
+            e = rel_fro(got, ref)
+            assert e <= TOL_GRAD_RELFRO, (name, "whole head", e)
+            worst["dkdv_tail"] = max(worst["dkdv_tail"], e)
+    print(f"\n{cid}: worst O {worst['o']:.4g} L {worst['l']:.3g} dQ-rows {worst['dq']:.3g} dK/dV {worst['dkdv_tail']:.3g}")
