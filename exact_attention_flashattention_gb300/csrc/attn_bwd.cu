@@ -11,7 +11,13 @@
 //   dP^T = V_j dO_i^T     SS-MMA  -> TMEM [384,512)   (dS^T written over it)
 //   dV  += P^T dO_i       TS-MMA  (A = P^T from TMEM) -> TMEM [0,128)
 //   dK  += dS^T Q_i       TS-MMA  (A = dS^T from TMEM) -> TMEM [128,256)
-//   dQ_i = dS K_j         SS-MMA  (A = dS from shared memory) -> TMEM [256,384)
+//   dQ_i^T = K_j^T dS^T   SS-MMA  (d = 128; dS^T from shared memory) -> TMEM [384,512)
+//   dQ_i   = dS K_j       SS-MMA  (d = 64, same operands swapped)      -> TMEM [384,448)
+// dS is stored already multiplied by the softmax scale, so dK and the dQ
+// partials need no further scaling.  With d = 128 the dQ partial comes out
+// transposed (head dimension on the TMEM lanes): a warp's FP32 reductions into
+// the accumulator then cover 32 consecutive floats of one row (a full 128-byte
+// line) instead of 16 bytes of 32 different rows.
 // The transposes follow from the equations: dV = P^T dO and dK = dS^T Q need
 // P^T and dS^T as the left operand, which the tensor core can read straight
 // from TMEM when the scores are computed with keys on the lanes.
@@ -30,15 +36,15 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPanelBytes = 128 * 128;
 
 // ---------------------------------------------------------------- preprocess
-// ndelta_r = -sum_c dO[r,c] O[r,c] (FP32, the negated D of the backward
-// equations), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.  The main kernel adds
-// the negated values inside packed FP32 pairs.
+// ndelta_r = -scale * sum_c dO[r,c] O[r,c] (FP32: the negated D of the
+// backward equations, times the softmax scale that the main kernel folds into
+// dS), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.
 // A group of D/8 threads handles one row; each thread reads 16 bytes of O and dO.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ delta,
                                                       float* __restrict__ lse2, float4* __restrict__ dq_acc,
-                                                      long rows) {
+                                                      long rows, float scale) {
     constexpr int TPR = D / 8;
     const long total = rows * TPR;
     const long stride = (long)gridDim.x * blockDim.x;
@@ -69,7 +75,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
         dq_acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
         dq_acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (part == 0) {
-            delta[row] = -acc;
+            delta[row] = -acc * scale;
             lse2[row] = -lse[row] * kLog2e;
         }
     }
@@ -205,6 +211,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint32_t dp_addr = tmem + lane_base + L::kTmemDP + 64 * half;
         uint8_t* ds_panel = smem + L::kDS + half * kPanelBytes;
         const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+        const uint64_t sc2 = f2_pack(scale, scale);
         uint32_t g = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -252,7 +259,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_before();
                     mbar_arrive(&bars[L::kBarPReady]);
 
-                    // dS^T = P^T o (dP^T - D): into TMEM (A operand of dK) and shared memory (dQ)
+                    // scale dS^T = P^T o (scale dP^T - scale D): into TMEM (A operand of dK) and shared
+                    // memory (an operand of the dQ product)
                     if (!mbar_wait(&bars[L::kBarDpFull], g & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
                     if (!mbar_wait(&bars[L::kBarDqFull], (g & 1) ^ 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
                     tc_fence_after();
@@ -265,8 +273,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const float2 dl = nd[16 * c + e];
-                            const uint64_t t = f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
-                                                      f2_pack(dl.x, dl.y));
+                            const uint64_t t = f2_fma(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])),
+                                                      sc2, f2_pack(dl.x, dl.y));
                             const uint64_t ds = f2_mul(f2_pack(p[32 * c + 2 * e], p[32 * c + 2 * e + 1]), t);
                             float d0, d1;
                             f2_unpack(ds, d0, d1);
@@ -302,22 +310,37 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const int i = w.i0 + it;
                     if (!mbar_wait(&bars[L::kBarDqFull], g & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
                     tc_fence_after();
-                    float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
+                    if constexpr (D == 128) {
+                        // dQ_i^T: this thread holds column `row` (a head-dimension index) of dQ_i for
+                        // all 128 query rows; one warp instruction covers 32 consecutive floats of a row.
+                        float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128) * D + row;
 #pragma unroll
-                    for (int h = 0; h < D / 64; ++h) {
-                        uint32_t r[64];
-                        tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                        tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                        tmem_wait_ld();
-                        if (h == D / 64 - 1) {
-                            tc_fence_before();
-                            mbar_arrive(&bars[L::kBarDqFree]);
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t r[64];
+                            tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                            tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h + 32,
+                                      *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                            tmem_wait_ld();
+                            if (h == 1) {
+                                tc_fence_before();
+                                mbar_arrive(&bars[L::kBarDqFree]);
+                            }
+#pragma unroll
+                            for (int e = 0; e < 64; ++e) red_add_f32(dst + (size_t)(64 * h + e) * D, __uint_as_float(r[e]));
                         }
+                    } else {
+                        // dQ_i: this thread holds query row `row`.
+                        float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
+                        uint32_t r[64];
+                        tmem_ld32(tmem + lane_base + L::kTmemDQ, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tmem_ld32(tmem + lane_base + L::kTmemDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        mbar_arrive(&bars[L::kBarDqFree]);
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            red_add_v4(dst + 64 * h + 4 * e, __uint_as_float(r[4 * e]) * scale,
-                                       __uint_as_float(r[4 * e + 1]) * scale, __uint_as_float(r[4 * e + 2]) * scale,
-                                       __uint_as_float(r[4 * e + 3]) * scale);
+                            red_add_v4(dst + 4 * e, __uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
+                                       __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
                     }
                 }
                 if (!ok) break;
@@ -327,7 +350,6 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     const uint32_t src = tmem + lane_base + (which ? L::kTmemDK : L::kTmemDV);
-                    const float mul = which ? scale : 1.f;
                     uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow * D * 2;
 #pragma unroll 1
                     for (int c = 0; c < D; c += 32) {
@@ -337,7 +359,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         uint32_t pk[16];
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * mul, __uint_as_float(r[2 * e + 1]) * mul);
+                            pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
                         for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -353,7 +375,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
             constexpr uint32_t kIdescG = idesc_f16(128, D, BF16, false, true);      // dV, dK (A in TMEM)
-            constexpr uint32_t kIdescQ = idesc_f16(128, D, BF16, true, true);       // dQ (A = dS, MN-major)
+            constexpr uint32_t kIdescQ = idesc_f16(128, D == 128 ? 128 : D, BF16, true, true);  // dQ^T or dQ
             const uint32_t k_base = smem_u32(smem + L::kK), v_base = smem_u32(smem + L::kV);
             const uint32_t q_base = smem_u32(smem + L::kQ), do_base = smem_u32(smem + L::kDO);
             const uint32_t ds_base = smem_u32(smem + L::kDS);
@@ -411,11 +433,15 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(&bars[L::kBarQEmpty + st]);
-                        // dQ_i = dS K_j (A = dS from shared memory, MN-major; B = K_j MN-major)
+                        // d = 128: dQ_i^T = K_j^T dS^T (A = K_j read MN-major, B = dS^T MN-major).
+                        // d = 64:  dQ_i = dS K_j (A = dS^T read MN-major, B = K_j MN-major).
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ss(tmem + L::kTmemDQ, sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024),
-                                   sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024), kIdescQ, kk > 0);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t kd = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
+                            const uint64_t sd = sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024);
+                            if constexpr (D == 128) mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
+                            else mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
+                        }
                         mma_commit(&bars[L::kBarDqFull]);
                     }
                     if (!ok) break;
@@ -501,7 +527,7 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         if (blocks > cap) blocks = cap;
         bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
             static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, a.delta, a.lse2,
-            reinterpret_cast<float4*>(a.dq_acc), rows);
+            reinterpret_cast<float4*>(a.dq_acc), rows, a.scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

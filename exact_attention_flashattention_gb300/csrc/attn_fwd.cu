@@ -39,7 +39,7 @@ template <int D>
 struct FwdLayout {
     static constexpr int kTile = 128 * D * 2;          // bytes of a 128-row tile
     static constexpr int kPanels = D / 64;
-    static constexpr int kStages = (D == 128) ? 3 : 6;  // K/V ring depth
+    static constexpr int kStages = (D == 128) ? 4 : 6;  // K/V ring depth
     static constexpr int kQ0 = 0;
     static constexpr int kQ1 = kTile;
     static constexpr int kKV = 2 * kTile;

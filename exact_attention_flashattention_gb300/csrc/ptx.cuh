@@ -282,6 +282,9 @@ template <int N> __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+__device__ __forceinline__ void red_add_f32(float* gaddr, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(a) : "memory");
+}
 __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
     asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
                  ::"l"(gaddr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
