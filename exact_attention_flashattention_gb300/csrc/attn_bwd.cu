@@ -296,7 +296,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else if (warp < 12) {
         // ------------------------------------------------------ dQ drain, dK/dV epilogue
-        regs_dec<112>();
+        regs_inc<144>();
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t g = 0;
@@ -312,22 +312,19 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tc_fence_after();
                     if constexpr (D == 128) {
                         // dQ_i^T: this thread holds column `row` (a head-dimension index) of dQ_i for
-                        // all 128 query rows; one warp instruction covers 32 consecutive floats of a row.
+                        // all 128 query rows; one warp instruction covers 32 consecutive floats of a
+                        // row.  The whole tile is read out of TMEM (and its columns released to the
+                        // next dP^T) before the reductions are issued.
                         float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128) * D + row;
+                        uint32_t r[128];
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t r[64];
-                            tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                            tmem_ld32(tmem + lane_base + L::kTmemDQ + 64 * h + 32,
-                                      *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
-                            tmem_wait_ld();
-                            if (h == 1) {
-                                tc_fence_before();
-                                mbar_arrive(&bars[L::kBarDqFree]);
-                            }
+                        for (int c = 0; c < 4; ++c)
+                            tmem_ld32(tmem + lane_base + L::kTmemDQ + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&r[32 * c]));
+                        tmem_wait_ld();
+                        tc_fence_before();
+                        mbar_arrive(&bars[L::kBarDqFree]);
 #pragma unroll
-                            for (int e = 0; e < 64; ++e) red_add_f32(dst + (size_t)(64 * h + e) * D, __uint_as_float(r[e]));
-                        }
+                        for (int e = 0; e < 128; ++e) red_add_f32(dst + (size_t)e * D, __uint_as_float(r[e]));
                     } else {
                         // dQ_i: this thread holds query row `row`.
                         float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
@@ -370,7 +367,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else {
-        regs_dec<112>();  // warps 12-15; the split 2x144 + 112 + 112 warpgroups uses 65536 registers
+        regs_dec<80>();  // warps 12-15; the split 2x144 + 144 + 80 warpgroups uses 65536 registers
         if (warp == 12 && lane == 0) {
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T

@@ -17,8 +17,9 @@
 //   WG1 (warps 4-7)   softmax for Q tile 1
 //   WG2 (warps 8-11)  O correction (lazy rescale) and the epilogue
 //   WG3 warp 12       single-thread tcgen05.mma issuer (also owns TMEM)
-//   WG3 warp 13       TMA producer (Q tiles, K/V ring)
-//   WG3 warps 14-15   idle
+//   WG3 warp 13       TMA producer, K/V ring
+//   WG3 warp 14       TMA producer, Q tiles
+//   WG3 warp 15       idle
 // TMEM (512 columns x 128 lanes): S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..).
 // Packed 16-bit P_q overwrites the first 64 columns of S_q.
 // Shared memory: Q0, Q1 (128 x d each) and a ring of K/V tiles (128 x d),
@@ -414,9 +415,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // Every MMA issued above completes before TMEM is released.
             mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
-        } else if (warp == 13 && lane == 0) {
-            // ------------------------------------------------------------ TMA producer
-            uint32_t tok = 0;
+        } else if (warp == 14 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer: Q tiles
+            // (its own warp, so that the K/V stream below never waits for a Q buffer to free up)
             int k = 0;
             bool ok = true;
             int last_q_item = -1;
@@ -430,6 +431,15 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tma_load_3d(smem + L::kQ0 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t0 * 128, w.bh);
                     tma_load_3d(smem + L::kQ1 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t1 * 128, w.bh);
                 }
+            }
+            // Let every copy issued above land before shared memory is released.
+            if (last_q_item >= 0) mbar_wait_drain(&bars[L::kBarQFull], last_q_item & 1, kWaitLimitNs);
+        } else if (warp == 13 && lane == 0) {
+            // ------------------------------------------------------------ TMA producer: K/V ring
+            uint32_t tok = 0;
+            bool ok = true;
+            WorkItem w;
+            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units);) {
                 for (int j = 0; j < w.n1 && ok; ++j) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
@@ -450,7 +460,6 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
             }
             // Let every copy issued above land before shared memory is released.
-            if (last_q_item >= 0) mbar_wait_drain(&bars[L::kBarQFull], last_q_item & 1, kWaitLimitNs);
             for (uint32_t t = (tok > (uint32_t)L::kStages ? tok - L::kStages : 0); t < tok; ++t)
                 mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
         }
