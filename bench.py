@@ -346,6 +346,8 @@ def run_ours(args):
     if rank != 0:
         return 0
 
+    props = torch.cuda.get_device_properties(dev)
+    n_sm = props.multi_processor_count
     peaks, peak_src = load_peaks()
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -384,6 +386,13 @@ def run_ours(args):
         "fwd_pct_peak": 100.0 * fwd_tf / peak_burst,
         "bwd_pct_peak": 100.0 * bwd_tf / peak_burst,
         "pct_peak_basis": f"bf16_tflops (burst) = {peak_burst} TFLOP/s, {peak_src}",
+        "fwd_pct_sustained_peak": 100.0 * fwd_tf / peak_sus,
+        "bwd_pct_sustained_peak": 100.0 * bwd_tf / peak_sus,
+        "nominal_peak_at_clock": (None if not clocks else {
+            "tflops": n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12, "sms": n_sm, "sm_mhz": clocks["sm_mhz"],
+            "basis": "SMs x 8192 dense bf16 FLOP/clk/SM (one 128x256x16 MMA per 128 cycles) x median SM clock",
+            "fwd_pct": 100.0 * fwd_tf / (n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12),
+            "bwd_pct": 100.0 * bwd_tf / (n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12)}),
         "kernel_ms": {"attn_fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms, "bwd_dq_convert": conv_ms},
         "roofline": {
             "kernel": "attn_bwd_kernel<128,bf16> (backward main)",
@@ -405,6 +414,71 @@ def run_ours(args):
     return 0
 
 
+SWEEP = [
+    # name, B, H, N, d, causal, dtype, sigma_qk
+    ("tiny B=1 H=2 N=128 d=64 causal", 1, 2, 128, 64, True, "bf16", 1.0),
+    ("tiny B=1 H=2 N=128 d=64 non-causal", 1, 2, 128, 64, False, "bf16", 1.0),
+    ("causal B=8 H=16 N=4096 d=128", 8, 16, 4096, 128, True, "bf16", 1.0),
+    ("non-causal B=4 H=16 N=4096 d=128", 4, 16, 4096, 128, False, "bf16", 1.0),
+    ("non-causal B=2 H=16 N=8192 d=128", 2, 16, 8192, 128, False, "bf16", 1.0),
+    ("non-causal B=1 H=16 N=16384 d=128", 1, 16, 16384, 128, False, "bf16", 1.0),
+    ("fp16 causal B=4 H=16 N=1024 d=64", 4, 16, 1024, 64, True, "fp16", 1.0),
+    ("fp16 causal B=4 H=16 N=2048 d=64", 4, 16, 2048, 64, True, "fp16", 1.0),
+    ("fp16 causal B=4 H=16 N=4096 d=64", 4, 16, 4096, 64, True, "fp16", 1.0),
+    ("stress causal B=1 H=32 N=32768 d=128 sigma_qk=2", 1, 32, 32768, 128, True, "bf16", 2.0),
+]
+
+
+def run_sweep(iters=20):
+    """Forward and backward TFLOPS of every workload of the list (CUDA events,
+    3 warm-up calls, `iters` timed calls each).  One JSON line per workload;
+    not the bench contract line."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import exact_attention_flashattention_gb300 as attn
+    from exact_attention_flashattention_gb300 import flops as F
+    peaks, src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    for name, B, H, N, d, causal, dtype, sig in SWEEP:
+        tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
+        g = torch.Generator(device=dev)
+        g.manual_seed(7)
+        q, k = ((torch.randn((B, H, N, d), generator=g, device=dev) * sig).to(tdt) for _ in range(2))
+        v, do = (torch.randn((B, H, N, d), generator=g, device=dev).to(tdt) for _ in range(2))
+        o, lse = torch.empty_like(q), torch.empty((B, H, N), device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        sc = d ** -0.5
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(iters):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / iters
+
+        fms = timed(lambda: attn.attn_fwd(q, k, v, o, lse, sc, causal, stream))
+        bms = timed(lambda: attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, sc, causal, stream))
+        if attn.attn_last_device_error(stream) != 0:
+            raise RuntimeError("device error word set")
+        ftf = F.fwd_flops(B, H, N, d, causal) / fms / 1e9
+        btf = F.bwd_flops(B, H, N, d, causal) / bms / 1e9
+        print(json.dumps({"sweep": name, "dtype": dtype, "fwd_ms": fms, "fwd_tflops": ftf,
+                          "fwd_pct_peak": 100 * ftf / burst, "bwd_ms": bms, "bwd_tflops": btf,
+                          "bwd_pct_peak": 100 * btf / burst, "peak_basis": f"bf16 burst {burst} ({src})"}),
+              flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -413,6 +487,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="print fwd / bwd TFLOPS of every workload of the list instead of the bench line")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,d[,noncausal] instead of the default workload (smaller cases for profiling)")
     args = ap.parse_args()
@@ -425,6 +501,8 @@ def main():
                          .format("causal" if WORKLOAD["causal"] else "non-causal", **WORKLOAD))
     if args.warmup < 3:
         args.warmup = 3
+    if args.sweep:
+        return run_sweep()
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
