@@ -296,7 +296,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else if (warp < 12) {
         // ------------------------------------------------------ dQ drain, dK/dV epilogue
-        regs_inc<144>();
+        // d = 128 holds a whole 128-column dQ^T tile in registers; d = 64 needs fewer.
+        if constexpr (D == 128) regs_inc<144>(); else regs_dec<112>();
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t g = 0;
@@ -367,7 +368,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else {
-        regs_dec<80>();  // warps 12-15; the split 2x144 + 144 + 80 warpgroups uses 65536 registers
+        // warps 12-15; the split 2 x 144 + 144 + 80 (d = 128) or 2 x 144 + 112 + 112 (d = 64)
+        // uses exactly the 65536 registers the block is launched with
+        if constexpr (D == 128) regs_dec<80>(); else regs_dec<112>();
         if (warp == 12 && lane == 0) {
             // ------------------------------------------------------ MMA issuer
             constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
@@ -379,6 +382,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t g = 0;
             int k = 0;
             bool ok = true;
+            constexpr bool kDqAfterS = (D == 64);
+            // d = 128: dQ_i^T = K_j^T dS^T (A = K_j read MN-major, B = dS^T MN-major).
+            // d = 64:  dQ_i = dS K_j (A = dS^T read MN-major, B = K_j MN-major).
+            // Reads the dS tile in shared memory; writes the dP^T columns (dK has read dS^T there).
+            auto issue_dq = [&]() {
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t kd = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
+                    const uint64_t sd = sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024);
+                    if constexpr (D == 128) mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
+                    else mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
+                }
+                mma_commit(&bars[L::kBarDqFull]);
+            };
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
@@ -399,6 +416,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    sdesc_sw128(qs + off, 16, 1024), kIdescS, kk > 0);
                         }
                         mma_commit(&bars[L::kBarSFull]);
+                        // d = 64: the previous query tile's dQ goes between S^T and dP^T, so the
+                        // elementwise P^T pass overlaps it as well as dP^T.  d = 128: it stays at the
+                        // end of the previous tile, where S^T hides the longer drain of its reductions
+                        // (measured: 949 vs 877 TFLOPS at d = 128; 505 vs 532 at d = 64).
+                        if (kDqAfterS && it > 0) issue_dq();
                         // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
                         if (!mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
@@ -430,18 +452,10 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                                    sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
                         }
                         mma_commit(&bars[L::kBarQEmpty + st]);
-                        // d = 128: dQ_i^T = K_j^T dS^T (A = K_j read MN-major, B = dS^T MN-major).
-                        // d = 64:  dQ_i = dS K_j (A = dS^T read MN-major, B = K_j MN-major).
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t kd = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
-                            const uint64_t sd = sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024);
-                            if constexpr (D == 128) mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
-                            else mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
-                        }
-                        mma_commit(&bars[L::kBarDqFull]);
+                        if (!kDqAfterS) issue_dq();
                     }
                     if (!ok) break;
+                    if (kDqAfterS) issue_dq();  // the item's last dQ tile
                     mma_commit(&bars[L::kBarKEmpty]);
                     mma_commit(&bars[L::kBarDkvFull]);
                 }
