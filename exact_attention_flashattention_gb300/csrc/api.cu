@@ -79,8 +79,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 attn_status_t check_sizes(int B, int H, int N, int d) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    if (N % 128 != 0) return ATTN_ERR_UNSUPPORTED;
-    const long long total = (long long)B * H * N * d;
+    const long long n_pad = ((long long)N + 127) / 128 * 128;
+    const long long total = (long long)B * H * n_pad * d;
     if (total >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
 }
@@ -92,7 +92,8 @@ struct WsLayout {
 };
 WsLayout ws_layout(int B, int H, int N, int d) {
     WsLayout w;
-    const size_t rows = (size_t)B * H * N;
+    // N_pad = 128 ceil(N / 128) rows per head, so the kernels may move whole 128-row tiles
+    const size_t rows = (size_t)B * H * (((size_t)N + 127) / 128 * 128);
     w.delta = 0;
     w.lse2 = align_up(w.delta + rows * 4, 256);
     w.dq_acc = align_up(w.lse2 + rows * 4, 256);
@@ -231,7 +232,7 @@ const char* attn_status_string(attn_status_t s) {
     switch (s) {
         case ATTN_OK: return "ATTN_OK";
         case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: null pointer, non-positive size or bad dtype";
-        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: d must be 64 or 128, N a multiple of 128";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: d must be 64 or 128 and B*H*N*d below 2^31";
         case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT: pointers must be 16-byte aligned (workspace 256)";
         case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
         case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA: a CUDA call failed";

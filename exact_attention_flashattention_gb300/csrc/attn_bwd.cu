@@ -38,56 +38,72 @@ constexpr int kPanelBytes = 128 * 128;
 // ---------------------------------------------------------------- preprocess
 // ndelta_r = -scale * sum_c dO[r,c] O[r,c] (FP32: the negated D of the
 // backward equations, times the softmax scale that the main kernel folds into
-// dS), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.
-// A group of D/8 threads handles one row; each thread reads 16 bytes of O and dO.
+// dS), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.  The three workspace arrays
+// hold N_pad = 128 ceil(N / 128) rows per head; the padding rows of a ragged
+// last tile get nlse2 = -inf (so P = 0 there) and ndelta = 0.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ delta,
                                                       float* __restrict__ lse2, float4* __restrict__ dq_acc,
-                                                      long rows, float scale) {
+                                                      long BH, int N, int N_pad, float scale) {
     constexpr int TPR = D / 8;
-    const long total = rows * TPR;
+    const long total = BH * N_pad * TPR;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const uint4 a = __ldg(o + i);
-        const uint4 b = __ldg(dout + i);
-        const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-        const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
+        const long prow = i / TPR;          // padded row
+        const int part = (int)(i % TPR);
+        const long bh = prow / N_pad;
+        const int n = (int)(prow % N_pad);
+        const bool valid = n < N;
         float acc = 0.f;
+        if (valid) {
+            const long src = (bh * N + n) * TPR + part;
+            const uint4 a = __ldg(o + src);
+            const uint4 b = __ldg(dout + src);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float2 fa, fb;
-            if constexpr (BF16) {
-                fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
-                fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
-            } else {
-                fa = __half22float2(*reinterpret_cast<const __half2*>(&av[e]));
-                fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
+            for (int e = 0; e < 4; ++e) {
+                float2 fa, fb;
+                if constexpr (BF16) {
+                    fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+                    fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
+                } else {
+                    fa = __half22float2(*reinterpret_cast<const __half2*>(&av[e]));
+                    fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
+                }
+                acc = fmaf(fa.x, fb.x, acc);
+                acc = fmaf(fa.y, fb.y, acc);
             }
-            acc = fmaf(fa.x, fb.x, acc);
-            acc = fmaf(fa.y, fb.y, acc);
         }
+        // The TPR threads of a row are consecutive lanes of one warp and all take the same branch.
         const unsigned mask = __activemask();
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
-        const long row = i / TPR;
-        const int part = (int)(i % TPR);
         dq_acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
         dq_acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (part == 0) {
-            delta[row] = -acc * scale;
-            lse2[row] = -lse[row] * kLog2e;
+            delta[prow] = valid ? -acc * scale : 0.f;
+            lse2[prow] = valid ? -lse[bh * N + n] * kLog2e : -INFINITY;
         }
     }
 }
 
 // ---------------------------------------------------------------- dQ convert
-template <bool BF16>
+// dq[bh, n, :] = 16-bit(dq_acc[bh, n, :]) for n < N (the accumulator has N_pad rows per head).
+template <int D, bool BF16>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                                         long n8) {
+                                                         long BH, int N, int N_pad) {
+    constexpr int PER_ROW = D / 8;   // 8 values (one uint4 of output) per thread
+    const long n8 = BH * N * PER_ROW;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
-        const float4 a = acc[2 * i], b = acc[2 * i + 1];
+        const long row = i / PER_ROW;
+        const int part = (int)(i % PER_ROW);
+        const long bh = row / N;
+        const int n = (int)(row % N);
+        const long src = ((bh * N_pad + n) * PER_ROW + part) * 2;
+        const float4 a = acc[src], b = acc[src + 1];
         dq[i] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
     }
 }
@@ -172,7 +188,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = N / 128;
+    const int T = (N + 127) / 128;  // the last tile is ragged when N % 128 != 0
+    const int N_pad = T * 128;      // rows per head of the workspace arrays
     const int n_units = BH * bwd_units_per_head(T, causal);
 
     if (threadIdx.x == 0) {
@@ -247,6 +264,11 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             for (int e = 0; e < 64; ++e)
                                 if (row > 64 * half + e) p[e] = 0.f;
                         }
+                        if (w.j * 128 + row >= N) {
+                            // a key past N in the ragged last tile (read as zeros)
+#pragma unroll
+                            for (int e = 0; e < 64; ++e) p[e] = 0.f;
+                        }
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
                             uint32_t pk[16];
@@ -316,7 +338,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // all 128 query rows; one warp instruction covers 32 consecutive floats of a
                         // row.  The whole tile is read out of TMEM (and its columns released to the
                         // next dP^T) before the reductions are issued.
-                        float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128) * D + row;
+                        float* dst = dq_acc + ((size_t)w.bh * N_pad + (size_t)i * 128) * D + row;
                         uint32_t r[128];
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -328,7 +350,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 128; ++e) red_add_f32(dst + (size_t)e * D, __uint_as_float(r[e]));
                     } else {
                         // dQ_i: this thread holds query row `row`.
-                        float* dst = dq_acc + ((size_t)w.bh * N + (size_t)i * 128 + row) * D;
+                        float* dst = dq_acc + ((size_t)w.bh * N_pad + (size_t)i * 128 + row) * D;
                         uint32_t r[64];
                         tmem_ld32(tmem + lane_base + L::kTmemDQ, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                         tmem_ld32(tmem + lane_base + L::kTmemDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
@@ -344,6 +366,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!ok) break;
                 if (!mbar_wait(&bars[L::kBarDkvFull], k & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
                 tc_fence_after();
+                const bool row_valid = w.j * 128 + row < N;
                 const size_t grow = (size_t)w.bh * N + (size_t)w.j * 128 + row;
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
@@ -358,9 +381,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
                             pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
+                        if (row_valid) {
+                            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                            for (int e = 0; e < 4; ++e)
+                                d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
                     }
                 }
                 tc_fence_before();
@@ -480,7 +506,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     tma_load_3d(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
                                 64 * p, i * 128, w.bh);
                 }
-                const size_t r0 = (size_t)w.bh * N + (size_t)i * 128;
+                const size_t r0 = (size_t)w.bh * N_pad + (size_t)i * 128;
                 bulk_load(smem + L::kVec + st * 1024, nlse2 + r0, 512, &bars[L::kBarQFull + st]);
                 bulk_load(smem + L::kVec + st * 1024 + 512, ndelta + r0, 512, &bars[L::kBarQFull + st]);
                 ++g;
@@ -529,16 +555,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 template <int D, bool BF16>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     using L = BwdLayout<D>;
-    const long rows = (long)a.BH * a.N;
+    const int T = (a.N + 127) / 128;
+    const int N_pad = T * 128;
     // 1. preprocess
     if (stage < 0 || stage == 0) {
-        const long threads_needed = rows * (D / 8);
+        const long threads_needed = (long)a.BH * N_pad * (D / 8);
         long blocks = (threads_needed + 255) / 256;
         const long cap = (long)a.num_sms * 8;
         if (blocks > cap) blocks = cap;
         bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
             static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, a.delta, a.lse2,
-            reinterpret_cast<float4*>(a.dq_acc), rows, a.scale);
+            reinterpret_cast<float4*>(a.dq_acc), (long)a.BH, a.N, N_pad, a.scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -554,7 +581,6 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         auto kern = attn_bwd_kernel<D, BF16>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
-        const int T = a.N / 128;
         const long n_units = (long)a.BH * (a.causal ? (T + 1) / 2 : T);
         const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
         kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
@@ -564,12 +590,12 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     }
     // 3. dQ conversion
     if (stage < 0 || stage == 2) {
-        const long n8 = rows * D / 8;
+        const long n8 = (long)a.BH * a.N * (D / 8);
         long blocks = (n8 + 255) / 256;
         const long cap = (long)a.num_sms * 8;
         if (blocks > cap) blocks = cap;
-        dq_convert_kernel<BF16><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
-                                                                 static_cast<uint4*>(a.dq), n8);
+        dq_convert_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
+                                                                    static_cast<uint4*>(a.dq), (long)a.BH, a.N, N_pad);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

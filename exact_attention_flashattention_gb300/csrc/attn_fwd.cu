@@ -133,7 +133,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = N / 128;
+    const int T = (N + 127) / 128;  // the last tile is ragged when N % 128 != 0
     const int M = (T + 1) / 2;
     const int n_units = BH * fwd_units_per_head(M, causal);
 
@@ -199,11 +199,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32(s_addr + 64, *reinterpret_cast<uint32_t(*)[32]>(&s[64]));
                 tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
                 tmem_wait_ld();
-                if (j == diag) {
-                    // key index > query index is masked (aligned top-left causal mask)
+                // Masked columns c > lim: on the diagonal tile a key index above the query index
+                // (aligned top-left causal mask); in a ragged last tile the keys past N (read as
+                // zeros).
+                int lim = 127;
+                if (j == diag) lim = row;
+                if (j == T - 1) lim = min(lim, N - 1 - j * 128);
+                if (lim < 127) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
-                        if (c > row) s[c] = __float_as_uint(-INFINITY);
+                        if (c > lim) s[c] = __float_as_uint(-INFINITY);
                 }
                 float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -325,14 +330,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-                    if (t < T) {
+                    if (grow < N) {
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                     }
                 }
-                if (t < T) lse_out[(size_t)w.bh * N + grow] = (mrow + log2f(l)) * kLn2;
+                if (grow < N) lse_out[(size_t)w.bh * N + grow] = (mrow + log2f(l)) * kLn2;
                 tc_fence_before();
             }
         }
@@ -480,7 +485,7 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     auto kern = attn_fwd_kernel<D, BF16>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    const int T = a.N / 128;
+    const int T = (a.N + 127) / 128;
     const int M = (T + 1) / 2;
     const long n_units = (long)a.BH * (a.causal ? (M + 1) / 2 : M);
     const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);

@@ -21,9 +21,11 @@
  *  - Q, K, V, O, dO, dQ, dK, dV are contiguous [B, H, N, d] arrays of 16-bit
  *    floats (bfloat16, or float16 for the *_ex calls with ATTN_FP16), row
  *    d fastest.  L (lse) is a contiguous FP32 [B, H, N] array, natural log.
- *  - Supported sizes: d in {64, 128}; N >= 128 and N % 128 == 0; B, H >= 1;
- *    B*H*N*d < 2^31.  Every pointer must be 16-byte aligned.  Anything else
- *    returns an error code before any work is queued.
+ *  - Supported sizes: d in {64, 128}; any N >= 1 (a last tile of fewer than
+ *    128 rows is handled with zero-filled loads and masking); B, H >= 1;
+ *    B*H*N_pad*d < 2^31 with N_pad = 128 ceil(N / 128).  Every pointer must be
+ *    16-byte aligned.  Anything else returns an error code before any work is
+ *    queued.
  *  - Outputs are overwritten, never accumulated.
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *    default stream).  A status of ATTN_OK means the work was queued.  Launch
@@ -50,7 +52,7 @@ extern "C" {
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID_ARG = 1,  /* null pointer, non-positive size, bad dtype   */
-    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, N % 128 != 0, too large  */
+    ATTN_ERR_UNSUPPORTED = 2,  /* d not in {64,128}, or too large             */
     ATTN_ERR_ALIGNMENT = 3,    /* a pointer not 16-byte aligned                */
     ATTN_ERR_WORKSPACE = 4,    /* workspace NULL or smaller than required      */
     ATTN_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed             */
@@ -74,8 +76,8 @@ ATTN_API attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, 
 
 /*
  * Bytes of device workspace attn_bwd needs: the D vector and L*log2(e)
- * (FP32 [B,H,N] each) and the FP32 dQ accumulator [B,H,N,d].  Returns 0 for
- * sizes attn_bwd would reject.
+ * (FP32 [B,H,N_pad] each) and the FP32 dQ accumulator [B,H,N_pad,d], with
+ * N_pad = 128 ceil(N / 128).  Returns 0 for sizes attn_bwd would reject.
  */
 ATTN_API size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 

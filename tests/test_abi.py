@@ -53,13 +53,17 @@ def test_argument_checks_before_any_launch(lib):
     null = vp(0)
     assert lib.attn_fwd(null, p, p, p, p, 1, 1, 128, 128, 1.0, 1, null) == 1          # INVALID_ARG
     assert lib.attn_fwd(p, p, p, p, p, 1, 1, 128, 96, 1.0, 1, null) == 2              # d unsupported
-    assert lib.attn_fwd(p, p, p, p, p, 1, 1, 100, 128, 1.0, 1, null) == 2             # N % 128
+    assert lib.attn_fwd(p, p, p, p, p, 1, 1, 0, 128, 1.0, 1, null) == 1               # N <= 0
+    assert lib.attn_fwd(p, p, p, p, p, 1 << 15, 1 << 15, 256, 128, 1.0, 1, null) == 2  # too large
     assert lib.attn_fwd(p, p, p, p, p, 0, 1, 128, 128, 1.0, 1, null) == 1             # B <= 0
     assert lib.attn_fwd(vp(258), p, p, p, p, 1, 1, 128, 128, 1.0, 1, null) == 3       # alignment
     assert lib.attn_fwd_ex(p, p, p, p, p, 1, 1, 128, 128, 1.0, 1, 7, null) == 1       # bad dtype
     ws = attn.attn_bwd_workspace_size(1, 1, 128, 128)
     assert ws >= 128 * 4 * 2 + 128 * 128 * 4 and ws % 256 == 0
-    assert attn.attn_bwd_workspace_size(1, 1, 100, 128) == 0
+    # any N: the workspace rows are padded to whole 128-row tiles
+    assert attn.attn_bwd_workspace_size(1, 1, 100, 128) == attn.attn_bwd_workspace_size(1, 1, 128, 128)
+    assert attn.attn_bwd_workspace_size(1, 1, 129, 64) == attn.attn_bwd_workspace_size(1, 1, 256, 64)
+    assert attn.attn_bwd_workspace_size(1, 1, 0, 64) == 0
     assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, null, 0, 1, 1, 128, 128, 1.0, 1, null) == 4   # workspace
     assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, vp(512), ws - 1, 1, 1, 128, 128, 1.0, 1, null) == 4
     assert lib.attn_bwd(p, p, p, p, p, p, p, p, p, vp(512 + 16), ws, 1, 1, 128, 128, 1.0, 1, null) == 3

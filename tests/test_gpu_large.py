@@ -36,6 +36,9 @@ CONFIGS = [
     ("fp16_causal_b4h16n2048d64", 4, 16, 2048, 64, True, "fp16", 1.0),
     ("fp16_causal_b4h16n4096d64", 4, 16, 4096, 64, True, "fp16", 1.0),
     ("stress_b1h32n32768d128", 1, 32, 32768, 128, True, "bf16", 2.0),
+    # N not a multiple of 128
+    ("ragged_causal_b2h16n4000d128", 2, 16, 4000, 128, True, "bf16", 1.0),
+    ("ragged_noncausal_b2h8n3001d64", 2, 8, 3001, 64, False, "fp16", 1.0),
 ]
 SEED = 20261202
 
@@ -54,7 +57,7 @@ def _sample_heads(BH):
 
 
 def _sample_rows(N, rng):
-    rows = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1}
+    rows = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1, (N - 1) // 128 * 128}
     rows.update(int(x) for x in rng.integers(0, N, size=22))
     return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
 

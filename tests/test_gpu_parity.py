@@ -28,6 +28,14 @@ SMALL = [
     (1, 2, 640, 64, True, "fp16"),
     (1, 2, 256, 64, False, "fp16"),
     (1, 1, 1024, 128, True, "bf16"),
+    # N not a multiple of 128: ragged last tile (zero-filled loads, masked keys, unstored rows)
+    (1, 2, 1, 128, True, "bf16"),
+    (1, 2, 1, 64, False, "bf16"),
+    (2, 2, 77, 64, True, "bf16"),
+    (1, 3, 200, 128, False, "bf16"),
+    (1, 2, 333, 128, True, "bf16"),
+    (2, 1, 257, 128, True, "fp16"),
+    (1, 2, 1000, 64, False, "fp16"),
 ]
 
 
