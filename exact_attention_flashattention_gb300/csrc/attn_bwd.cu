@@ -397,8 +397,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // warps 12-15; the split 2 x 144 + 144 + 80 (d = 128) or 2 x 144 + 112 + 112 (d = 64)
         // uses exactly the 65536 registers the block is launched with
         if constexpr (D == 128) regs_dec<80>(); else regs_dec<112>();
-        if (warp == 12 && lane == 0) {
-            // ------------------------------------------------------ MMA issuer
+        if (warp == 12) {
+            // ------------------------------------------------------ MMA issuer (the whole warp; lane 0 issues)
             constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
             constexpr uint32_t kIdescG = idesc_f16(128, D, BF16, false, true);      // dV, dK (A in TMEM)
             constexpr uint32_t kIdescQ = idesc_f16(128, D == 128 ? 128 : D, BF16, true, true);  // dQ^T or dQ
@@ -417,76 +417,76 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t kd = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
                     const uint64_t sd = sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024);
-                    if constexpr (D == 128) mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
-                    else mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
+                    if constexpr (D == 128) warp_mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
+                    else warp_mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
                 }
-                mma_commit(&bars[L::kBarDqFull]);
+                warp_mma_commit(&bars[L::kBarDqFull]);
             };
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
                     if (!bwd_item(u, sidx, T, causal, w)) break;
-                    if (!mbar_wait(&bars[L::kBarKFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                    if (!mbar_wait(&bars[L::kBarVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    if (!warp_mbar_wait(&bars[L::kBarKFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    if (!warp_mbar_wait(&bars[L::kBarVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     tc_fence_after();
                     for (int it = 0; it < w.n; ++it, ++g) {
                         const uint32_t st = g & 1;
                         const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
-                        if (!mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (!warp_mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
                         // S^T = K_j Q_i^T (its TMEM columns were last read by the previous dV, issued earlier)
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024),
+                            warp_mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024),
                                    sdesc_sw128(qs + off, 16, 1024), kIdescS, kk > 0);
                         }
-                        mma_commit(&bars[L::kBarSFull]);
+                        warp_mma_commit(&bars[L::kBarSFull]);
                         // d = 64: the previous query tile's dQ goes between S^T and dP^T, so the
                         // elementwise P^T pass overlaps it as well as dP^T.  d = 128: it stays at the
                         // end of the previous tile, where S^T hides the longer drain of its reductions
                         // (measured: 949 vs 877 TFLOPS at d = 128; 505 vs 532 at d = 64).
                         if (kDqAfterS && it > 0) issue_dq();
                         // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
-                        if (!mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (!warp_mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024),
+                            warp_mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024),
                                    sdesc_sw128(dos + off, 16, 1024), kIdescS, kk > 0);
                         }
-                        mma_commit(&bars[L::kBarDpFull]);
-                        if (it == w.n - 1) mma_commit(&bars[L::kBarVEmpty]);
+                        warp_mma_commit(&bars[L::kBarDpFull]);
+                        if (it == w.n - 1) warp_mma_commit(&bars[L::kBarVEmpty]);
                         // dV += P^T dO_i
-                        if (!mbar_wait(&bars[L::kBarPReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                        if (it == 0 && !mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (!warp_mbar_wait(&bars[L::kBarPReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (it == 0 && !warp_mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                            mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol,
+                            warp_mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol,
                                    sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
                         }
                         // dK += dS^T Q_i
-                        if (!mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (!warp_mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
                             const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                            mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol,
+                            warp_mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol,
                                    sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
                         }
-                        mma_commit(&bars[L::kBarQEmpty + st]);
+                        warp_mma_commit(&bars[L::kBarQEmpty + st]);
                         if (!kDqAfterS) issue_dq();
                     }
                     if (!ok) break;
                     if (kDqAfterS) issue_dq();  // the item's last dQ tile
-                    mma_commit(&bars[L::kBarKEmpty]);
-                    mma_commit(&bars[L::kBarDkvFull]);
+                    warp_mma_commit(&bars[L::kBarKEmpty]);
+                    warp_mma_commit(&bars[L::kBarDkvFull]);
                 }
             }
-            mma_commit(&bars[L::kBarTeardown]);
+            warp_mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
         } else if (warp == 13 && lane == 0) {
             // ------------------------------------------------------ TMA producer

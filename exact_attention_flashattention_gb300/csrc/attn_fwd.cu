@@ -343,8 +343,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
     } else {
         regs_dec<88>();  // warps 12-15; the split 2x176 + 72 + 88 warpgroups uses 65536 registers
-        if (warp == 12 && lane == 0) {
-            // ------------------------------------------------------------ MMA issuer
+        if (warp == 12) {
+            // ------------------------------------------------------------ MMA issuer (the whole warp; lane 0 issues)
             constexpr uint32_t kIdescQK = idesc_f16(128, 128, BF16, false, false);
             constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, false, true);
             const uint32_t q_base[2] = {smem_u32(smem + L::kQ0), smem_u32(smem + L::kQ1)};
@@ -358,7 +358,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
                     const uint64_t a = sdesc_sw128(q_base[q] + off, 16, 1024);
                     const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + off, 16, 1024);
-                    mma_ss(d_tmem, a, b, kIdescQK, kk > 0);
+                    warp_mma_ss(d_tmem, a, b, kIdescQK, kk > 0);
                 }
             };
             auto issue_pv = [&](int q, uint32_t slot, bool acc) {
@@ -367,28 +367,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                     const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + kk * 2048, kPanelBytes, 1024);
-                    mma_ts(d_tmem, p_tmem + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
+                    warp_mma_ts(d_tmem, p_tmem + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
                 }
             };
             auto wait_kv = [&](uint32_t& slot) -> bool {
                 slot = tok % L::kStages;
-                const bool r = mbar_wait(&bars[L::kBarKVFull + slot], (tok / L::kStages) & 1, guard, kDevTimeoutMma);
+                const bool r = warp_mbar_wait(&bars[L::kBarKVFull + slot], (tok / L::kStages) & 1, guard, kDevTimeoutMma);
                 ++tok;
                 tc_fence_after();
                 return r;
             };
             WorkItem w;
             for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units);) {
-                if (!mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
+                if (!warp_mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
                 q_phase ^= 1;
                 tc_fence_after();
                 uint32_t kslot;
                 if (!wait_kv(kslot)) { ok = false; break; }
                 issue_qk(0, kslot);
-                mma_commit(&bars[L::kBarSFull + 0]);
+                warp_mma_commit(&bars[L::kBarSFull + 0]);
                 issue_qk(1, kslot);
-                mma_commit(&bars[L::kBarSFull + 1]);
-                mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                warp_mma_commit(&bars[L::kBarSFull + 1]);
+                warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
                 for (int j = 0; j < w.n1 && ok; ++j) {
                     uint32_t vslot;
                     if (!wait_kv(vslot)) { ok = false; break; }
@@ -397,28 +397,28 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     for (int q = 0; q < 2; ++q) {
                         const int n = q ? w.n1 : w.n0;
                         if (j >= n) continue;
-                        if (!mbar_wait(&bars[L::kBarPVReady + q], pv_phase[q], guard, kDevTimeoutMma)) { ok = false; break; }
+                        if (!warp_mbar_wait(&bars[L::kBarPVReady + q], pv_phase[q], guard, kDevTimeoutMma)) { ok = false; break; }
                         pv_phase[q] ^= 1;
                         tc_fence_after();
                         issue_pv(q, vslot, j > 0);
-                        mma_commit(&bars[L::kBarODone + q]);
+                        warp_mma_commit(&bars[L::kBarODone + q]);
                         if (j + 1 < n) {
                             if (!have_k) {
                                 if (!wait_kv(kslot)) { ok = false; break; }
                                 have_k = true;
                             }
                             issue_qk(q, kslot);
-                            mma_commit(&bars[L::kBarSFull + q]);
+                            warp_mma_commit(&bars[L::kBarSFull + q]);
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&bars[L::kBarKVEmpty + vslot]);
-                    if (have_k) mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                    warp_mma_commit(&bars[L::kBarKVEmpty + vslot]);
+                    if (have_k) warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
                 }
-                mma_commit(&bars[L::kBarQEmpty]);
+                warp_mma_commit(&bars[L::kBarQEmpty]);
             }
             // Every MMA issued above completes before TMEM is released.
-            mma_commit(&bars[L::kBarTeardown]);
+            warp_mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
         } else if (warp == 14 && lane == 0) {
             // ------------------------------------------------------------ TMA producer: Q tiles
