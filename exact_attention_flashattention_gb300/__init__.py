@@ -8,10 +8,15 @@ Names mirror the C ABI:
     attn_fwd(q, k, v, o, lse, scale, causal, stream=None)
     attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream=None)
     attn_bwd_workspace_size(B, H, N, d)
+    attn_fwd_layout(q, k, v, o, lse, scale, causal, layout, cu_seqlens=None, max_seqlen=None, stream=None)
+    attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, layout, ...)
+    attn_bwd_layout_workspace_size(B, H, max_seqlen, d, layout, total_tokens)
     attn_last_device_error(stream=None)
 plus two allocating conveniences, ``forward`` and ``backward``.
-Tensors are contiguous CUDA tensors [B, H, N, d] of bfloat16 or float16; lse
-is float32 [B, H, N].
+Tensors are contiguous CUDA tensors of bfloat16 or float16: [B, H, N, d] (layout
+"bhsd", the default), [B, N, H, d] ("bshd") or [total_tokens, H, d] ("packed",
+with int32 device offsets cu_seqlens [B + 1]); lse is float32 [B, H, N], or
+[H, total_tokens] when packed.
 """
 from __future__ import annotations
 
@@ -21,7 +26,8 @@ import threading
 
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_stage", "attn_bwd_workspace_size", "attn_last_device_error",
-    "attn_status_string", "attn_last_launch_count", "forward", "backward", "library_path", "load",
+    "attn_status_string", "attn_last_launch_count", "attn_fwd_layout", "attn_bwd_layout",
+    "attn_bwd_layout_workspace_size", "LAYOUTS", "forward", "backward", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -31,10 +37,12 @@ _lib = None
 
 ATTN_OK = 0
 ATTN_BF16, ATTN_FP16 = 0, 1
+LAYOUTS = {"bhsd": 0, "bshd": 1, "packed": 2}
 
 EXPORTS = (
     "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex", "attn_bwd_stage",
-    "attn_status_string", "attn_last_device_error", "attn_last_launch_count",
+    "attn_status_string", "attn_last_device_error", "attn_last_launch_count", "attn_fwd_layout",
+    "attn_bwd_layout", "attn_bwd_layout_workspace_size", "attn_bwd_noalloc",
 )
 
 
@@ -67,11 +75,16 @@ def load():
         lib.attn_bwd_stage.argtypes = [i] + [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, vp]
         lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
         lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_fwd_layout.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, f, i, i, i, vp, i, vp]
+        lib.attn_bwd_layout.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, i, vp, i, vp]
+        lib.attn_bwd_layout_workspace_size.argtypes = [i, i, i, i, i, i]
+        lib.attn_bwd_layout_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_last_device_error.argtypes = [vp]
         lib.attn_last_launch_count.argtypes = []
         for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_bwd_stage,
+                   lib.attn_fwd_layout, lib.attn_bwd_layout,
                    lib.attn_last_device_error,
                    lib.attn_last_launch_count):
             fn.restype = ctypes.c_int
@@ -148,6 +161,55 @@ def attn_bwd_stage(stage: int, q, k, v, o, dout, lse, dq, dk, dv, workspace, sca
         raise AttnError(st, f"attn_bwd_stage({stage})")
 
 
+def _layout_dims(q, layout, cu_seqlens, max_seqlen):
+    """(B, H, max_seqlen, d, layout code, offsets pointer, total_tokens) of a call."""
+    if layout not in LAYOUTS:
+        raise ValueError(f"layout must be one of {sorted(LAYOUTS)}")
+    if layout == "bhsd":
+        B, H, N, d = q.shape
+        return B, H, N, d, 0, None, 0
+    if layout == "bshd":
+        B, N, H, d = q.shape
+        return B, H, N, d, 1, None, B * N
+    import torch
+    if cu_seqlens is None or max_seqlen is None:
+        raise ValueError("layout 'packed' needs cu_seqlens and max_seqlen")
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    total, H, d = q.shape
+    return cu_seqlens.numel() - 1, H, int(max_seqlen), d, 2, _check(cu_seqlens, "cu_seqlens"), total
+
+
+def attn_fwd_layout(q, k, v, o, lse, scale: float, causal: bool, layout: str, cu_seqlens=None, max_seqlen=None,
+                    stream=None) -> None:
+    """Queue the forward pass for a layout of LAYOUTS (tensor shapes in the module docstring)."""
+    lib = load()
+    B, H, N, d, lc, cu, total = _layout_dims(q, layout, cu_seqlens, max_seqlen)
+    st = lib.attn_fwd_layout(_check(q, "q"), _check(k, "k"), _check(v, "v"), _check(o, "o"), _check(lse, "lse"),
+                             B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), lc, cu, total,
+                             _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_fwd_layout")
+
+
+def attn_bwd_layout_workspace_size(B: int, H: int, max_seqlen: int, d: int, layout: str, total_tokens: int = 0) -> int:
+    return int(load().attn_bwd_layout_workspace_size(B, H, max_seqlen, d, LAYOUTS[layout], total_tokens))
+
+
+def attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool, layout: str,
+                    cu_seqlens=None, max_seqlen=None, stream=None) -> None:
+    """Queue the backward pass for a layout of LAYOUTS."""
+    lib = load()
+    B, H, N, d, lc, cu, total = _layout_dims(q, layout, cu_seqlens, max_seqlen)
+    st = lib.attn_bwd_layout(_check(q, "q"), _check(k, "k"), _check(v, "v"), _check(o, "o"), _check(dout, "dout"),
+                             _check(lse, "lse"), _check(dq, "dq"), _check(dk, "dk"), _check(dv, "dv"),
+                             _check(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+                             B, H, N, d, float(scale), int(bool(causal)), _dtype_code(q), lc, cu, total,
+                             _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_bwd_layout")
+
+
 def attn_last_device_error(stream=None) -> int:
     return int(load().attn_last_device_error(_stream_handle(stream)))
 
@@ -156,24 +218,38 @@ def attn_last_launch_count() -> int:
     return int(load().attn_last_launch_count())
 
 
-def forward(q, k, v, scale=None, causal=False, stream=None):
+def forward(q, k, v, scale=None, causal=False, stream=None, layout="bhsd", cu_seqlens=None, max_seqlen=None):
     """Allocate O and L, queue the forward pass, return (O, L)."""
     import torch
     d = q.shape[-1]
     scale = d ** -0.5 if scale is None else scale
     o = torch.empty_like(q)
-    lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
-    attn_fwd(q, k, v, o, lse, scale, causal, stream)
+    if layout == "bhsd":
+        lse = torch.empty(q.shape[:-1], dtype=torch.float32, device=q.device)
+        attn_fwd(q, k, v, o, lse, scale, causal, stream)
+        return o, lse
+    if layout == "bshd":
+        B, N, H, _ = q.shape
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    else:
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=q.device)
+    attn_fwd_layout(q, k, v, o, lse, scale, causal, layout, cu_seqlens, max_seqlen, stream)
     return o, lse
 
 
-def backward(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None, stream=None):
+def backward(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None, stream=None, layout="bhsd",
+             cu_seqlens=None, max_seqlen=None):
     """Allocate dQ, dK, dV (and the workspace if not given), queue the backward pass."""
     import torch
-    B, H, N, d = q.shape
+    B, H, N, d, _, _, total = _layout_dims(q, layout, cu_seqlens, max_seqlen)
     scale = d ** -0.5 if scale is None else scale
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     if workspace is None:
-        workspace = torch.empty(attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
-    attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+        workspace = torch.empty(attn_bwd_layout_workspace_size(B, H, N, d, layout, total), dtype=torch.uint8,
+                                device=q.device)
+    if layout == "bhsd":
+        attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, stream)
+    else:
+        attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, layout, cu_seqlens, max_seqlen,
+                        stream)
     return dq, dk, dv

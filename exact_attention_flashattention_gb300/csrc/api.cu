@@ -74,15 +74,66 @@ bool make_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
     return r == CUDA_SUCCESS;
 }
 
+// [tokens, H, d] 16-bit tensor (BSHD, or packed sequences), box {64, 1, 128}: the same
+// 128 rows x 128 bytes in shared memory as the heads-major box.
+bool make_map_tokens(CUtensorMap* m, const void* base, int H, int tokens, int d) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, 1, 128};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool make_map_seq(CUtensorMap* m, const void* base, const SeqDesc& s, int d) {
+    return s.token_major ? make_map_tokens(m, base, s.H, s.tokens, d) : make_map(m, base, s.B * s.H, s.N, d);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-attn_status_t check_sizes(int B, int H, int N, int d) {
+size_t n_pad_of(int N) { return ((size_t)N + 127) / 128 * 128; }
+
+// Rows of each backward workspace array: B H blocks of N_pad rows, or for packed sequences
+// H blocks of 128 (ceil(tokens / 128) + B) rows (seq_ws_base in seq.cuh).
+size_t ws_rows(const SeqDesc& s) {
+    return s.cu != nullptr ? (size_t)s.H * 128 * (((size_t)s.tokens + 127) / 128 + (size_t)s.B)
+                           : (size_t)s.B * s.H * n_pad_of(s.N);
+}
+
+// Checks the sizes and layout arguments and fills the sequence descriptor (error word unset).
+attn_status_t check_seq(int B, int H, int N, int d, attn_layout_t layout, const int* cu_seqlens, int total_tokens,
+                        SeqDesc& s) {
     if (B <= 0 || H <= 0 || N <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (layout != ATTN_LAYOUT_BHSD && layout != ATTN_LAYOUT_BSHD && layout != ATTN_LAYOUT_PACKED)
+        return ATTN_ERR_INVALID_ARG;
+    const bool packed = layout == ATTN_LAYOUT_PACKED;
+    if (packed != (cu_seqlens != nullptr)) return ATTN_ERR_INVALID_ARG;
+    if (packed && total_tokens < 0) return ATTN_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
-    const long long n_pad = ((long long)N + 127) / 128 * 128;
-    const long long total = (long long)B * H * n_pad * d;
-    if (total >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    if (packed && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u) != 0) return ATTN_ERR_ALIGNMENT;
+    s.cu = cu_seqlens;
+    s.B = B;
+    s.H = H;
+    s.N = N;
+    s.token_major = layout != ATTN_LAYOUT_BHSD;
+    s.tokens = packed ? total_tokens : 0;
+    s.error = nullptr;
+    if (layout == ATTN_LAYOUT_BSHD) {
+        if ((long long)B * N >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+        s.tokens = B * N;
+    }
+    if ((long long)ws_rows(s) * d >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
     return ATTN_OK;
+}
+
+// The fixed-length layout's checks (existing entry points).
+attn_status_t check_sizes(int B, int H, int N, int d) {
+    SeqDesc s;
+    return check_seq(B, H, N, d, ATTN_LAYOUT_BHSD, nullptr, 0, s);
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -90,15 +141,20 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 struct WsLayout {
     size_t delta, lse2, dq_acc, total;
 };
-WsLayout ws_layout(int B, int H, int N, int d) {
+WsLayout ws_layout(const SeqDesc& s, int d) {
     WsLayout w;
-    // N_pad = 128 ceil(N / 128) rows per head, so the kernels may move whole 128-row tiles
-    const size_t rows = (size_t)B * H * (((size_t)N + 127) / 128 * 128);
+    // whole 128-row tiles of every sequence fit, so the kernels always move full tiles
+    const size_t rows = ws_rows(s);
     w.delta = 0;
     w.lse2 = align_up(w.delta + rows * 4, 256);
     w.dq_acc = align_up(w.lse2 + rows * 4, 256);
     w.total = align_up(w.dq_acc + rows * (size_t)d * 4, 256);
     return w;
+}
+WsLayout ws_layout(int B, int H, int N, int d) {
+    SeqDesc s;
+    check_seq(B, H, N, d, ATTN_LAYOUT_BHSD, nullptr, 0, s);
+    return ws_layout(s, d);
 }
 
 }  // namespace
@@ -108,26 +164,30 @@ using namespace gb300;
 
 extern "C" {
 
-attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
-                          int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+attn_status_t attn_fwd_layout(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int max_seqlen, int d, float scale, int causal, attn_dtype_t dtype,
+                              attn_layout_t layout, const int* cu_seqlens, int total_tokens, void* stream) {
     t_last_launches = 0;
     if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
-    attn_status_t st = check_sizes(B, H, N, d);
+    SeqDesc seq;
+    attn_status_t st = check_seq(B, H, max_seqlen, d, layout, cu_seqlens, total_tokens, seq);
     if (st != ATTN_OK) return st;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_ALIGNMENT;
+    if (seq.token_major && seq.tokens == 0) return ATTN_OK;  // packed, every sequence empty: nothing to do
     DevInfo di;
     if (!dev_info(di)) return ATTN_ERR_CUDA;
+    seq.error = di.err_ptr;
     FwdArgs a;
     std::memset(&a, 0, sizeof(a));
-    const int BH = B * H;
-    if (!make_map(&a.tm_q, q, BH, N, d) || !make_map(&a.tm_k, k, BH, N, d) || !make_map(&a.tm_v, v, BH, N, d))
+    if (!make_map_seq(&a.tm_q, q, seq, d) || !make_map_seq(&a.tm_k, k, seq, d) || !make_map_seq(&a.tm_v, v, seq, d))
         return ATTN_ERR_CUDA;
     a.o = o;
     a.lse = lse;
-    a.BH = BH;
-    a.N = N;
+    a.seq = seq;
+    a.BH = B * H;
+    a.N = max_seqlen;
     a.d = d;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
@@ -137,6 +197,11 @@ attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, 
     if (launch_fwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     t_last_launches = 1;
     return ATTN_OK;
+}
+
+attn_status_t attn_fwd_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N,
+                          int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+    return attn_fwd_layout(q, k, v, o, lse, B, H, N, d, scale, causal, dtype, ATTN_LAYOUT_BHSD, nullptr, 0, stream);
 }
 
 attn_status_t attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -149,31 +214,46 @@ size_t attn_bwd_workspace_size(int B, int H, int N, int d) {
     return ws_layout(B, H, N, d).total;
 }
 
+size_t attn_bwd_layout_workspace_size(int B, int H, int max_seqlen, int d, attn_layout_t layout,
+                                      int total_tokens) {
+    // the offsets themselves are not needed for the size; a dummy non-null pointer selects packed
+    static const int kDummy = 0;
+    SeqDesc s;
+    if (check_seq(B, H, max_seqlen, d, layout, layout == ATTN_LAYOUT_PACKED ? &kDummy : nullptr, total_tokens, s) !=
+        ATTN_OK)
+        return 0;
+    return ws_layout(s, d).total;
+}
+
 }  // extern "C"
 
 namespace {
 attn_status_t bwd_common(int stage, const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
-                         int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
+                         int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype,
+                         attn_layout_t layout, const int* cu_seqlens, int total_tokens, void* stream) {
     t_last_launches = 0;
     if (stage < -1 || stage > 2) return ATTN_ERR_INVALID_ARG;
     if (!q || !k || !v || !o || !dout || !lse || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
     if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
-    attn_status_t st = check_sizes(B, H, N, d);
+    SeqDesc seq;
+    attn_status_t st = check_seq(B, H, N, d, layout, cu_seqlens, total_tokens, seq);
     if (st != ATTN_OK) return st;
-    const WsLayout w = ws_layout(B, H, N, d);
+    const WsLayout w = ws_layout(seq, d);
     if (!workspace || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGNMENT;
     const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv};
     for (const void* p : ptrs)
         if (!aligned16(p)) return ATTN_ERR_ALIGNMENT;
+    if (seq.token_major && seq.tokens == 0) return ATTN_OK;  // packed, every sequence empty: nothing to do
     DevInfo di;
     if (!dev_info(di)) return ATTN_ERR_CUDA;
+    seq.error = di.err_ptr;
     BwdArgs a;
     std::memset(&a, 0, sizeof(a));
     const int BH = B * H;
-    if (!make_map(&a.tm_q, q, BH, N, d) || !make_map(&a.tm_k, k, BH, N, d) || !make_map(&a.tm_v, v, BH, N, d) ||
-        !make_map(&a.tm_do, dout, BH, N, d))
+    if (!make_map_seq(&a.tm_q, q, seq, d) || !make_map_seq(&a.tm_k, k, seq, d) || !make_map_seq(&a.tm_v, v, seq, d) ||
+        !make_map_seq(&a.tm_do, dout, seq, d))
         return ATTN_ERR_CUDA;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.o = o;
@@ -185,6 +265,8 @@ attn_status_t bwd_common(int stage, const void* q, const void* k, const void* v,
     a.delta = reinterpret_cast<float*>(ws + w.delta);
     a.lse2 = reinterpret_cast<float*>(ws + w.lse2);
     a.dq_acc = reinterpret_cast<float*>(ws + w.dq_acc);
+    a.ws_rows = (long)ws_rows(seq);
+    a.seq = seq;
     a.BH = BH;
     a.N = N;
     a.d = d;
@@ -206,7 +288,7 @@ attn_status_t attn_bwd_ex(const void* q, const void* k, const void* v, const voi
                           const float* lse, void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes,
                           int B, int H, int N, int d, float scale, int causal, attn_dtype_t dtype, void* stream) {
     return bwd_common(-1, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
-                      dtype, stream);
+                      dtype, ATTN_LAYOUT_BHSD, nullptr, 0, stream);
 }
 
 attn_status_t attn_bwd_stage(int stage, const void* q, const void* k, const void* v, const void* o,
@@ -218,7 +300,16 @@ attn_status_t attn_bwd_stage(int stage, const void* q, const void* k, const void
         return ATTN_ERR_INVALID_ARG;
     }
     return bwd_common(stage, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale,
-                      causal, dtype, stream);
+                      causal, dtype, ATTN_LAYOUT_BHSD, nullptr, 0, stream);
+}
+
+attn_status_t attn_bwd_layout(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                              const float* lse, void* dq, void* dk, void* dv, void* workspace,
+                              size_t workspace_bytes, int B, int H, int max_seqlen, int d, float scale, int causal,
+                              attn_dtype_t dtype, attn_layout_t layout, const int* cu_seqlens, int total_tokens,
+                              void* stream) {
+    return bwd_common(-1, q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, max_seqlen, d, scale,
+                      causal, dtype, layout, cu_seqlens, total_tokens, stream);
 }
 
 attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
@@ -231,7 +322,9 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
 const char* attn_status_string(attn_status_t s) {
     switch (s) {
         case ATTN_OK: return "ATTN_OK";
-        case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG: null pointer, non-positive size or bad dtype";
+        case ATTN_ERR_INVALID_ARG:
+            return "ATTN_ERR_INVALID_ARG: null pointer, non-positive size, bad dtype or layout, or (device) "
+                   "inconsistent sequence offsets";
         case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED: d must be 64 or 128 and B*H*N*d below 2^31";
         case ATTN_ERR_ALIGNMENT: return "ATTN_ERR_ALIGNMENT: pointers must be 16-byte aligned (workspace 256)";
         case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE: workspace missing or too small";
@@ -248,7 +341,9 @@ attn_status_t attn_last_device_error(void* stream) {
     if (v != 0) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
-        return v == kDevSmemAlign ? ATTN_ERR_CUDA : ATTN_ERR_TIMEOUT;
+        if (v == kDevSmemAlign) return ATTN_ERR_CUDA;
+        if (v == kDevBadSeqLen) return ATTN_ERR_INVALID_ARG;
+        return ATTN_ERR_TIMEOUT;
     }
     return ATTN_OK;
 }

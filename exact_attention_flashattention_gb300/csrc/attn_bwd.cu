@@ -27,6 +27,7 @@
 // and dK/dV epilogue, warp 12 MMA issuer (owns TMEM), warp 13 TMA producer.
 #include "attn_internal.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace gb300 {
 namespace {
@@ -39,25 +40,32 @@ constexpr int kPanelBytes = 128 * 128;
 // ndelta_r = -scale * sum_c dO[r,c] O[r,c] (FP32: the negated D of the
 // backward equations, times the softmax scale that the main kernel folds into
 // dS), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.  The three workspace arrays
-// hold N_pad = 128 ceil(N / 128) rows per head; the padding rows of a ragged
-// last tile get nlse2 = -inf (so P = 0 there) and ndelta = 0.
-template <int D, bool BF16>
+// hold, per (sequence, head) slice, its rows padded to whole 128-row tiles
+// (seq_ws_base); the padding rows of a ragged last tile get nlse2 = -inf (so
+// P = 0 there) and ndelta = 0.  Threads walk (slice, row < n_pad) with n_pad
+// the padded length of the longest sequence and skip rows past a slice's own.
+template <int D, bool BF16, bool kTM>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
                                                       const float* __restrict__ lse, float* __restrict__ delta,
                                                       float* __restrict__ lse2, float4* __restrict__ dq_acc,
-                                                      long BH, int N, int N_pad, float scale) {
+                                                      const SeqDesc seq, int n_pad, float scale) {
     constexpr int TPR = D / 8;
-    const long total = BH * N_pad * TPR;
+    const long total = (long)seq.B * seq.H * n_pad * TPR;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const long prow = i / TPR;          // padded row
+        const long prow = i / TPR;          // padded row of the longest sequence
         const int part = (int)(i % TPR);
-        const long bh = prow / N_pad;
-        const int n = (int)(prow % N_pad);
-        const bool valid = n < N;
+        const int bh = (int)(prow / n_pad);
+        const int n = (int)(prow % n_pad);
+        SeqItem si;
+        seq_item<kTM>(seq, bh, si);
+        // the TPR threads of a row are consecutive lanes of one warp and take the same branches
+        if (n >= (si.len + 127) / 128 * 128) continue;
+        const size_t wrow = seq_ws_base<kTM>(seq, si, n_pad) + n;
+        const bool valid = n < si.len;
         float acc = 0.f;
         if (valid) {
-            const long src = (bh * N + n) * TPR + part;
+            const size_t src = seq_row_offset<kTM>(seq, si, n, D) / 8 + part;
             const uint4 a = __ldg(o + src);
             const uint4 b = __ldg(dout + src);
             const uint32_t av[4] = {a.x, a.y, a.z, a.w};
@@ -76,35 +84,39 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
                 acc = fmaf(fa.y, fb.y, acc);
             }
         }
-        // The TPR threads of a row are consecutive lanes of one warp and all take the same branch.
         const unsigned mask = __activemask();
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
-        dq_acc[2 * i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dq_acc[2 * i + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * (wrow * TPR + part)] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dq_acc[2 * (wrow * TPR + part) + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (part == 0) {
-            delta[prow] = valid ? -acc * scale : 0.f;
-            lse2[prow] = valid ? -lse[bh * N + n] * kLog2e : -INFINITY;
+            delta[wrow] = valid ? -acc * scale : 0.f;
+            lse2[wrow] = valid ? -lse[seq_lse_index<kTM>(seq, si, n)] * kLog2e : -INFINITY;
         }
     }
 }
 
 // ---------------------------------------------------------------- dQ convert
-// dq[bh, n, :] = 16-bit(dq_acc[bh, n, :]) for n < N (the accumulator has N_pad rows per head).
-template <int D, bool BF16>
+// dq row n of each (sequence, head) slice = 16-bit(its accumulator row), for n below the
+// sequence's length; threads walk (slice, row < N) with N the longest length.
+template <int D, bool BF16, bool kTM>
 __global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                                         long BH, int N, int N_pad) {
+                                                         const SeqDesc seq, int n_pad) {
     constexpr int PER_ROW = D / 8;   // 8 values (one uint4 of output) per thread
-    const long n8 = BH * N * PER_ROW;
+    const long n8 = (long)seq.B * seq.H * seq.N * PER_ROW;
     const long stride = (long)gridDim.x * blockDim.x;
     for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
         const long row = i / PER_ROW;
         const int part = (int)(i % PER_ROW);
-        const long bh = row / N;
-        const int n = (int)(row % N);
-        const long src = ((bh * N_pad + n) * PER_ROW + part) * 2;
+        const int bh = (int)(row / seq.N);
+        const int n = (int)(row % seq.N);
+        SeqItem si;
+        seq_item<kTM>(seq, bh, si);
+        if (n >= si.len) continue;
+        const size_t src = ((seq_ws_base<kTM>(seq, si, n_pad) + n) * PER_ROW + part) * 2;
         const float4 a = acc[src], b = acc[src + 1];
-        dq[i] = make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
+        dq[seq_row_offset<kTM>(seq, si, n, D) / 8 + part] =
+            make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
     }
 }
 
@@ -138,39 +150,46 @@ struct BwdLayout {
 };
 
 struct BwdItem {
-    int bh, j, i0, n;   // head, key/value tile, first query tile, number of query tiles
+    SeqItem si;         // the (sequence, head) slice
+    int T;              // its number of 128-row tiles
+    int j, i0, n;       // key/value tile, first query tile, number of query tiles
 };
 
 // Work list.  Causal: units of two key/value tiles of one head, j and T-1-j, longest first.
 // Tile j meets T-j query tiles, so every unit holds T+1 of them and a static round-robin of
 // units over the persistent CTAs is balanced.  Non-causal: one tile per unit (all equally
 // long; a finer grain shortens the tail).  Consecutive units share a head, so the CTAs
-// running at one time reuse that head's Q / dO from L2.
+// running at one time reuse that head's Q / dO from L2.  Units are laid out for the longest
+// sequence (T tiles); a shorter packed sequence skips the units past its own tiles (slot 0
+// is skipped only when slot 1 is too, so the callers stop at the first skipped slot).
 __device__ __forceinline__ int bwd_units_per_head(int T, int causal) { return causal ? (T + 1) / 2 : T; }
 
-__device__ __forceinline__ bool bwd_item(int u, int s, int T, int causal, BwdItem& w) {
+template <bool kTM>
+__device__ __forceinline__ bool bwd_item(int u, int s, int T, int causal, const SeqDesc& seq, BwdItem& w) {
     const int uph = bwd_units_per_head(T, causal);
     const int jp = u % uph;
+    seq_item<kTM>(seq, u / uph, w.si);
+    w.T = (w.si.len + 127) / 128;
     if (causal) {
-        const int jl = T - 1 - jp;
+        const int jl = w.T - 1 - jp;
+        if (jl < jp) return false;
         if (s == 1 && jl == jp) return false;
         w.j = s ? jl : jp;
     } else {
-        if (s == 1) return false;
+        if (s == 1 || jp >= w.T) return false;
         w.j = jp;
     }
-    w.bh = u / uph;
     w.i0 = causal ? w.j : 0;
-    w.n = T - w.i0;
+    w.n = w.T - w.i0;
     return true;
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kTM>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ nlse2, const float* __restrict__ ndelta, float* __restrict__ dq_acc,
-                void* __restrict__ dk_out, void* __restrict__ dv_out, int BH, int N, float scale, int causal,
+                void* __restrict__ dk_out, void* __restrict__ dv_out, const SeqDesc seq, float scale, int causal,
                 int smem_slack, int* error) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -188,9 +207,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = (N + 127) / 128;  // the last tile is ragged when N % 128 != 0
-    const int N_pad = T * 128;      // rows per head of the workspace arrays
-    const int n_units = BH * bwd_units_per_head(T, causal);
+    const int T = (seq.N + 127) / 128;  // tiles of the longest sequence (the last one may be ragged)
+    const int N_pad = T * 128;          // rows per slice of the fixed-length workspace arrays
+    const int n_units = seq.B * seq.H * bwd_units_per_head(T, causal);
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < L::kNumBars; ++b) mbar_init(&bars[b], 1);
@@ -234,7 +253,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             for (int sidx = 0; sidx < 2 && ok; ++sidx) {
                 BwdItem w;
-                if (!bwd_item(u, sidx, T, causal, w)) break;
+                if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
                 for (int it = 0; it < w.n; ++it, ++g) {
                     const int i = w.i0 + it;
                     const bool diag = causal && i == w.j;
@@ -264,8 +283,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             for (int e = 0; e < 64; ++e)
                                 if (row > 64 * half + e) p[e] = 0.f;
                         }
-                        if (w.j * 128 + row >= N) {
-                            // a key past N in the ragged last tile (read as zeros)
+                        if (w.j * 128 + row >= w.si.len) {
+                            // a key past the end of the sequence in its ragged last tile
 #pragma unroll
                             for (int e = 0; e < 64; ++e) p[e] = 0.f;
                         }
@@ -328,7 +347,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
             for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                 BwdItem w;
-                if (!bwd_item(u, sidx, T, causal, w)) break;
+                if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
                 for (int it = 0; it < w.n; ++it, ++g) {
                     const int i = w.i0 + it;
                     if (!mbar_wait(&bars[L::kBarDqFull], g & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
@@ -338,7 +357,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // all 128 query rows; one warp instruction covers 32 consecutive floats of a
                         // row.  The whole tile is read out of TMEM (and its columns released to the
                         // next dP^T) before the reductions are issued.
-                        float* dst = dq_acc + ((size_t)w.bh * N_pad + (size_t)i * 128) * D + row;
+                        float* dst = dq_acc + (seq_ws_base<kTM>(seq, w.si, N_pad) + (size_t)i * 128) * D + row;
                         uint32_t r[128];
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
@@ -350,7 +369,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 128; ++e) red_add_f32(dst + (size_t)e * D, __uint_as_float(r[e]));
                     } else {
                         // dQ_i: this thread holds query row `row`.
-                        float* dst = dq_acc + ((size_t)w.bh * N_pad + (size_t)i * 128 + row) * D;
+                        float* dst = dq_acc + (seq_ws_base<kTM>(seq, w.si, N_pad) + (size_t)i * 128 + row) * D;
                         uint32_t r[64];
                         tmem_ld32(tmem + lane_base + L::kTmemDQ, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
                         tmem_ld32(tmem + lane_base + L::kTmemDQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
@@ -366,12 +385,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (!ok) break;
                 if (!mbar_wait(&bars[L::kBarDkvFull], k & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
                 tc_fence_after();
-                const bool row_valid = w.j * 128 + row < N;
-                const size_t grow = (size_t)w.bh * N + (size_t)w.j * 128 + row;
+                const bool row_valid = w.j * 128 + row < w.si.len;
+                const size_t grow_off = seq_row_offset<kTM>(seq, w.si, w.j * 128 + row, D);
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     const uint32_t src = tmem + lane_base + (which ? L::kTmemDK : L::kTmemDV);
-                    uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow * D * 2;
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(which ? dk_out : dv_out) + grow_off * 2;
 #pragma unroll 1
                     for (int c = 0; c < D; c += 32) {
                         uint32_t r[32];
@@ -425,7 +444,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
-                    if (!bwd_item(u, sidx, T, causal, w)) break;
+                    if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
                     if (!warp_mbar_wait(&bars[L::kBarKFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     if (!warp_mbar_wait(&bars[L::kBarVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     tc_fence_after();
@@ -501,12 +520,12 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 mbar_arrive_expect_tx(&bars[L::kBarQFull + st], 2 * L::kTile + 1024);
 #pragma unroll
                 for (int p = 0; p < L::kPanels; ++p) {
-                    tma_load_3d(smem + L::kQ + st * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + st],
-                                64 * p, i * 128, w.bh);
-                    tma_load_3d(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
-                                64 * p, i * 128, w.bh);
+                    seq_tma_load<kTM>(smem + L::kQ + st * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + st],
+                                 w.si, 64 * p, i * 128);
+                    seq_tma_load<kTM>(smem + L::kDO + st * L::kTile + p * kPanelBytes, &tm_do, &bars[L::kBarQFull + st],
+                                 w.si, 64 * p, i * 128);
                 }
-                const size_t r0 = (size_t)w.bh * N_pad + (size_t)i * 128;
+                const size_t r0 = seq_ws_base<kTM>(seq, w.si, N_pad) + (size_t)i * 128;
                 bulk_load(smem + L::kVec + st * 1024, nlse2 + r0, 512, &bars[L::kBarQFull + st]);
                 bulk_load(smem + L::kVec + st * 1024 + 512, ndelta + r0, 512, &bars[L::kBarQFull + st]);
                 ++g;
@@ -515,21 +534,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
-                    if (!bwd_item(u, sidx, T, causal, w)) break;
+                    if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
                     // V_j as soon as the previous item's last dP^T is done, then the first Q_i / dO_i,
                     // then K_j once the previous item's last dQ is done, then the rest.
                     if (!mbar_wait(&bars[L::kBarVEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bars[L::kBarVFull], L::kTile);
 #pragma unroll
                     for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_3d(smem + L::kV + p * kPanelBytes, &tm_v, &bars[L::kBarVFull], 64 * p, w.j * 128, w.bh);
+                        seq_tma_load<kTM>(smem + L::kV + p * kPanelBytes, &tm_v, &bars[L::kBarVFull], w.si, 64 * p, w.j * 128);
                     if (!load_q(w, 0)) { ok = false; break; }
                     if (!mbar_wait(&bars[L::kBarKEmpty], (k & 1) ^ 1, guard, kDevTimeoutLoad)) { ok = false; break; }
                     mbar_arrive_expect_tx(&bars[L::kBarKFull], L::kTile);
                     last_kv = k;
 #pragma unroll
                     for (int p = 0; p < L::kPanels; ++p)
-                        tma_load_3d(smem + L::kK + p * kPanelBytes, &tm_k, &bars[L::kBarKFull], 64 * p, w.j * 128, w.bh);
+                        seq_tma_load<kTM>(smem + L::kK + p * kPanelBytes, &tm_k, &bars[L::kBarKFull], w.si, 64 * p, w.j * 128);
                     for (int it = 1; it < w.n && ok; ++it)
                         if (!load_q(w, it)) ok = false;
                 }
@@ -552,20 +571,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kTM>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     using L = BwdLayout<D>;
     const int T = (a.N + 127) / 128;
     const int N_pad = T * 128;
     // 1. preprocess
     if (stage < 0 || stage == 0) {
-        const long threads_needed = (long)a.BH * N_pad * (D / 8);
+        const long threads_needed = (long)a.BH * N_pad * (D / 8);  // rows walked: every slice at the longest length
         long blocks = (threads_needed + 255) / 256;
         const long cap = (long)a.num_sms * 8;
         if (blocks > cap) blocks = cap;
-        bwd_pre_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(
+        bwd_pre_kernel<D, BF16, kTM><<<(int)blocks, 256, 0, stream>>>(
             static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, a.delta, a.lse2,
-            reinterpret_cast<float4*>(a.dq_acc), (long)a.BH, a.N, N_pad, a.scale);
+            reinterpret_cast<float4*>(a.dq_acc), a.seq, N_pad, a.scale);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -578,13 +597,13 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         const int smem_bytes = want < max_smem ? want : max_smem;
         const int slack = smem_bytes - L::kBytes;
         if (slack < 0) return cudaErrorInvalidConfiguration;
-        auto kern = attn_bwd_kernel<D, BF16>;
+        auto kern = attn_bwd_kernel<D, BF16, kTM>;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
         const long n_units = (long)a.BH * (a.causal ? (T + 1) / 2 : T);
         const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
         kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
-                                                      a.dk, a.dv, a.BH, a.N, a.scale, a.causal, slack, a.error);
+                                                      a.dk, a.dv, a.seq, a.scale, a.causal, slack, a.error);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
@@ -594,22 +613,27 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         long blocks = (n8 + 255) / 256;
         const long cap = (long)a.num_sms * 8;
         if (blocks > cap) blocks = cap;
-        dq_convert_kernel<D, BF16><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
-                                                                    static_cast<uint4*>(a.dq), (long)a.BH, a.N, N_pad);
+        dq_convert_kernel<D, BF16, kTM><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
+                                                                    static_cast<uint4*>(a.dq), a.seq, N_pad);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
+template <bool kTM>
+cudaError_t launch_bwd_l(const BwdArgs& a, cudaStream_t stream, int stage) {
+    if (a.d == 128)
+        return a.fp16 ? launch_bwd_t<128, false, kTM>(a, stream, stage) : launch_bwd_t<128, true, kTM>(a, stream, stage);
+    if (a.d == 64)
+        return a.fp16 ? launch_bwd_t<64, false, kTM>(a, stream, stage) : launch_bwd_t<64, true, kTM>(a, stream, stage);
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage) {
-    if (a.d == 128)
-        return a.fp16 ? launch_bwd_t<128, false>(a, stream, stage) : launch_bwd_t<128, true>(a, stream, stage);
-    if (a.d == 64)
-        return a.fp16 ? launch_bwd_t<64, false>(a, stream, stage) : launch_bwd_t<64, true>(a, stream, stage);
-    return cudaErrorInvalidValue;
+    return a.seq.token_major ? launch_bwd_l<true>(a, stream, stage) : launch_bwd_l<false>(a, stream, stage);
 }
 
 }  // namespace gb300

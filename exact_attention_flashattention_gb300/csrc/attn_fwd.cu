@@ -26,6 +26,7 @@
 // all in the 128-byte-swizzle layout written by TMA.
 #include "attn_internal.h"
 #include "ptx.cuh"
+#include "seq.cuh"
 
 namespace gb300 {
 namespace {
@@ -67,7 +68,9 @@ struct FwdLayout {
 };
 
 struct WorkItem {
-    int bh, m;        // head index, Q tile pair index
+    SeqItem si;       // the (sequence, head) slice
+    int T;            // its number of 128-row tiles
+    int m;            // Q tile pair index
     int t0, t1;       // Q tile indices
     int n0, n1;       // number of KV tiles for each Q tile
 };
@@ -76,10 +79,13 @@ struct WorkItem {
 // pair m meets 2m+1 and 2m+2 key/value tiles, so every unit holds the same amount of work and
 // a static round-robin of units over the persistent CTAs is balanced.  Non-causal: every item
 // is equally long, so each unit is one item (a finer grain shortens the tail).  Consecutive
-// units share a head, so the CTAs running at one time reuse its K / V from L2.
+// units share a head, so the CTAs running at one time reuse its K / V from L2.  With packed
+// sequences of different lengths the units are laid out for the longest one (M pairs per
+// slice) and the items past the end of a shorter sequence are skipped.
 __device__ __forceinline__ int fwd_units_per_head(int M, int causal) { return causal ? (M + 1) / 2 : M; }
 
-__device__ __forceinline__ bool fwd_item(int u, int s, int M, int T, int causal, WorkItem& w) {
+template <bool kTM>
+__device__ __forceinline__ bool fwd_item(int u, int s, int M, int causal, const SeqDesc& seq, WorkItem& w) {
     const int uph = fwd_units_per_head(M, causal);
     const int mp = u % uph;
     int m;
@@ -91,12 +97,14 @@ __device__ __forceinline__ bool fwd_item(int u, int s, int M, int T, int causal,
         if (s == 1) return false;
         m = M - 1 - mp;
     }
-    w.bh = u / uph;
+    seq_item<kTM>(seq, u / uph, w.si);
+    w.T = (w.si.len + 127) / 128;
     w.m = m;
     w.t0 = 2 * m;
     w.t1 = 2 * m + 1;
-    w.n0 = causal ? min(w.t0 + 1, T) : T;
-    w.n1 = causal ? min(w.t1 + 1, T) : T;
+    if (w.t0 >= w.T) return false;  // past the end of this sequence
+    w.n0 = causal ? min(w.t0 + 1, w.T) : w.T;
+    w.n1 = causal ? min(w.t1 + 1, w.T) : w.T;
     return true;
 }
 
@@ -105,21 +113,22 @@ __device__ __forceinline__ bool fwd_item(int u, int s, int M, int T, int causal,
 struct FwdIter {
     int pos;
     __device__ FwdIter() : pos(2 * (int)blockIdx.x) {}
-    __device__ bool next(WorkItem& w, int M, int T, int causal, int n_units) {
+    template <bool kTM>
+    __device__ bool next(WorkItem& w, int M, int causal, const SeqDesc& seq, int n_units) {
         for (;;) {
             const int u = pos >> 1, s = pos & 1;
             if (u >= n_units) return false;
             pos = s ? 2 * (u + (int)gridDim.x) : pos + 1;
-            if (fwd_item(u, s, M, T, causal, w)) return true;
+            if (fwd_item<kTM>(u, s, M, causal, seq, w)) return true;
         }
     }
 };
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kTM>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_out,
-                float* __restrict__ lse_out, int BH, int N, float scale, int causal, int* error) {
+                float* __restrict__ lse_out, const SeqDesc seq, float scale, int causal, int* error) {
     using L = FwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align the dynamic shared memory base to 1024 bytes (128B-swizzle atoms).
@@ -133,9 +142,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int T = (N + 127) / 128;  // the last tile is ragged when N % 128 != 0
+    const int T = (seq.N + 127) / 128;  // tiles of the longest sequence (the last one may be ragged)
     const int M = (T + 1) / 2;
-    const int n_units = BH * fwd_units_per_head(M, causal);
+    const int n_units = seq.B * seq.H * fwd_units_per_head(M, causal);
 
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::kBarQFull], 1);
@@ -184,10 +193,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int k = 0;
         bool ok = true;
         WorkItem w;
-        for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
+        for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
             const int t = q ? w.t1 : w.t0;
             const int n = q ? w.n1 : w.n0;
-            const int diag = (causal && t < T) ? t : -1;
+            const int diag = (causal && t < w.T) ? t : -1;
             float m_run = -INFINITY, l_run = 0.f;
             for (int j = 0; j < n; ++j) {
                 if (!mbar_wait(&bars[L::kBarSFull + q], s_phase, guard, kDevTimeoutSoftmax)) { ok = false; break; }
@@ -200,11 +209,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32(s_addr + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
                 tmem_wait_ld();
                 // Masked columns c > lim: on the diagonal tile a key index above the query index
-                // (aligned top-left causal mask); in a ragged last tile the keys past N (read as
-                // zeros).
+                // (aligned top-left causal mask); in a ragged last tile the keys past the end of the
+                // sequence (zeros, or rows of the next sequence).
                 int lim = 127;
                 if (j == diag) lim = row;
-                if (j == T - 1) lim = min(lim, N - 1 - j * 128);
+                if (j == w.T - 1) lim = min(lim, w.si.len - 1 - j * 128);
                 if (lim < 127) {
 #pragma unroll
                     for (int c = 0; c < 128; ++c)
@@ -275,7 +284,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int k = 0;
         bool ok = true;
         WorkItem w;
-        for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
+        for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
             for (int j = 0; j < w.n1 && ok; ++j) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
@@ -320,7 +329,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const int grow = t * 128 + row;
                 const float inv_l = 1.f / l;
                 const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
-                uint8_t* dst = reinterpret_cast<uint8_t*>(o_out) + ((size_t)w.bh * N + grow) * (size_t)D * 2;
+                uint8_t* dst = reinterpret_cast<uint8_t*>(o_out) + seq_row_offset<kTM>(seq, w.si, grow, D) * 2;
 #pragma unroll 1
                 for (int c = 0; c < D; c += 32) {
                     uint32_t r[32];
@@ -330,14 +339,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 16; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
-                    if (grow < N) {
+                    if (grow < w.si.len) {
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
                             d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                     }
                 }
-                if (grow < N) lse_out[(size_t)w.bh * N + grow] = (mrow + log2f(l)) * kLn2;
+                if (grow < w.si.len) lse_out[seq_lse_index<kTM>(seq, w.si, grow)] = (mrow + log2f(l)) * kLn2;
                 tc_fence_before();
             }
         }
@@ -378,7 +387,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 return r;
             };
             WorkItem w;
-            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units);) {
+            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units);) {
                 if (!warp_mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
                 q_phase ^= 1;
                 tc_fence_after();
@@ -427,14 +436,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             int last_q_item = -1;
             WorkItem w;
-            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units); ++k) {
+            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
                 if (k > 0 && !mbar_wait(&bars[L::kBarQEmpty], (k - 1) & 1, guard, kDevTimeoutLoad)) { ok = false; break; }
                 mbar_arrive_expect_tx(&bars[L::kBarQFull], 2 * L::kTile);
                 last_q_item = k;
 #pragma unroll
                 for (int p = 0; p < L::kPanels; ++p) {
-                    tma_load_3d(smem + L::kQ0 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t0 * 128, w.bh);
-                    tma_load_3d(smem + L::kQ1 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, w.t1 * 128, w.bh);
+                    seq_tma_load<kTM>(smem + L::kQ0 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], w.si, 64 * p, w.t0 * 128);
+                    seq_tma_load<kTM>(smem + L::kQ1 + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], w.si, 64 * p, w.t1 * 128);
                 }
             }
             // Let every copy issued above land before shared memory is released.
@@ -444,7 +453,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t tok = 0;
             bool ok = true;
             WorkItem w;
-            for (FwdIter itr; ok && itr.next(w, M, T, causal, n_units);) {
+            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units);) {
                 for (int j = 0; j < w.n1 && ok; ++j) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
@@ -458,8 +467,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const CUtensorMap* map = which ? &tm_v : &tm_k;
 #pragma unroll
                         for (int p = 0; p < L::kPanels; ++p)
-                            tma_load_3d(smem + L::kKV + slot * L::kTile + p * kPanelBytes, map,
-                                        &bars[L::kBarKVFull + slot], 64 * p, j * 128, w.bh);
+                            seq_tma_load<kTM>(smem + L::kKV + slot * L::kTile + p * kPanelBytes, map,
+                                         &bars[L::kBarKVFull + slot], w.si, 64 * p, j * 128);
                         ++tok;
                     }
                 }
@@ -478,11 +487,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool BF16>
+template <int D, bool BF16, bool kTM>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using L = FwdLayout<D>;
     const int smem_bytes = L::kBytes + 1024;  // + alignment slack
-    auto kern = attn_fwd_kernel<D, BF16>;
+    auto kern = attn_fwd_kernel<D, BF16, kTM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     const int T = (a.N + 127) / 128;
@@ -490,17 +499,22 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const long n_units = (long)a.BH * (a.causal ? (M + 1) / 2 : M);
     const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
     if (grid <= 0) return cudaSuccess;
-    kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.BH, a.N, a.scale,
-                                                  a.causal, a.error);
+    kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.seq, a.scale, a.causal,
+                                                  a.error);
     return cudaGetLastError();
+}
+
+template <bool kTM>
+cudaError_t launch_fwd_l(const FwdArgs& a, cudaStream_t stream) {
+    if (a.d == 128) return a.fp16 ? launch_fwd_t<128, false, kTM>(a, stream) : launch_fwd_t<128, true, kTM>(a, stream);
+    if (a.d == 64) return a.fp16 ? launch_fwd_t<64, false, kTM>(a, stream) : launch_fwd_t<64, true, kTM>(a, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-    if (a.d == 128) return a.fp16 ? launch_fwd_t<128, false>(a, stream) : launch_fwd_t<128, true>(a, stream);
-    if (a.d == 64) return a.fp16 ? launch_fwd_t<64, false>(a, stream) : launch_fwd_t<64, true>(a, stream);
-    return cudaErrorInvalidValue;
+    return a.seq.token_major ? launch_fwd_l<true>(a, stream) : launch_fwd_l<false>(a, stream);
 }
 
 }  // namespace gb300

@@ -16,17 +16,29 @@ enum DeviceError : int {
     kDevTimeoutSoftmax = 3,  // a softmax / elementwise warp's wait gave up
     kDevTimeoutCorr = 4,     // a correction / epilogue warp's wait gave up
     kDevSmemAlign = 5,       // dynamic shared memory could not be 1024-byte aligned (kernel did nothing)
+    kDevBadSeqLen = 6,       // packed sequences: offsets decreasing, past the tokens, or longer than the maximum
 };
 
 // Wait limit for every mbarrier wait in the kernels (nanoseconds of
 // %globaltimer).  No single wait in a healthy launch comes near it.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
+// Row layout of the sequence dimension (see seq.cuh for the addressing).
+struct SeqDesc {
+    const int* cu;    // device sequence offsets [B + 1], or nullptr when every sequence is N long
+    int B, H;
+    int N;            // sequence length, or the longest sequence when cu != nullptr
+    int token_major;  // 0: [B, H, N, d] (BHSD); 1: [tokens, H, d] (BSHD, or packed when cu != nullptr)
+    int tokens;       // rows of a token-major tensor: B N, or cu[B]
+    int* error;       // device error word (kDevBadSeqLen)
+};
+
 struct FwdArgs {
-    CUtensorMap tm_q, tm_k, tm_v;   // [BH, N, d], box {64, 128, 1}, 128B swizzle
-    void* o;          // [BH, N, d] 16-bit
-    float* lse;       // [BH, N]
-    int BH, N, d;
+    CUtensorMap tm_q, tm_k, tm_v;   // 16-bit, box of 64 columns x 128 rows, 128B swizzle
+    void* o;          // same layout as q, 16-bit
+    float* lse;       // [B, H, N], or [H, tokens] for packed sequences
+    SeqDesc seq;
+    int BH, N, d;     // BH = B H; N as in seq
     float scale;      // softmax scale applied to QK^T
     int causal;
     int fp16;         // 0 = bf16, 1 = fp16
@@ -36,15 +48,18 @@ struct FwdArgs {
 
 struct BwdArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;
-    const void* o;    // [BH, N, d]
-    const void* dout; // [BH, N, d]
-    const float* lse; // [BH, N]
-    void* dq;         // [BH, N, d]
+    const void* o;    // same layout as q
+    const void* dout; // same layout as q
+    const float* lse; // as FwdArgs::lse
+    void* dq;         // same layout as q
     void* dk;
     void* dv;
-    float* delta;     // workspace [BH, N]   -D = -rowsum(dO o O)
-    float* lse2;      // workspace [BH, N]   -L * log2(e)
-    float* dq_acc;    // workspace [BH, N, d] FP32
+    // workspace arrays, indexed by the rows of seq_ws_base (seq.cuh); ws_rows rows each
+    float* delta;     // -scale D = -scale rowsum(dO o O)
+    float* lse2;      // -L log2(e)
+    float* dq_acc;    // [ws_rows, d] FP32
+    long ws_rows;
+    SeqDesc seq;
     int BH, N, d;
     float scale;
     int causal;

@@ -62,6 +62,23 @@ typedef enum {
 typedef enum { ATTN_BF16 = 0, ATTN_FP16 = 1 } attn_dtype_t;
 
 /*
+ * Memory layout of Q, K, V, O, dO, dQ, dK, dV and L for the *_layout calls.
+ * The pages' kernels use [B, H, N, d] (ATTN_LAYOUT_BHSD, the layout of every
+ * call without "_layout").  "Dense B200 attention from scratch"
+ * (b200-attention, Appendix "Benchmark Calibration") also ships a direct-BSHD
+ * variant; the flash_attention_cuda README lists variable-length sequence
+ * packing among the features it leaves out.
+ *   ATTN_LAYOUT_BHSD    tensors [B, H, N, d];  L [B, H, N]
+ *   ATTN_LAYOUT_BSHD    tensors [B, N, H, d];  L [B, H, N]
+ *   ATTN_LAYOUT_PACKED  tensors [total_tokens, H, d] holding B sequences back
+ *                       to back: sequence b is rows cu_seqlens[b] ..
+ *                       cu_seqlens[b+1] - 1 (lengths may differ, may be 0);
+ *                       L [H, total_tokens].  Attention never crosses a
+ *                       sequence boundary; the causal mask is per sequence.
+ */
+typedef enum { ATTN_LAYOUT_BHSD = 0, ATTN_LAYOUT_BSHD = 1, ATTN_LAYOUT_PACKED = 2 } attn_layout_t;
+
+/*
  * Forward pass (the page's forward equations, section "Mathematical
  * Formulation").  Reads q, k, v [B,H,N,d]; writes o [B,H,N,d] and
  * lse [B,H,N] (L, natural log, FP32), which attn_bwd needs.  BF16 data.
@@ -73,6 +90,23 @@ ATTN_API attn_status_t attn_fwd(const void *q, const void *k, const void *v, voi
 ATTN_API attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, void *o, float *lse,
                           int B, int H, int N, int d, float scale, int causal,
                           attn_dtype_t dtype, void *stream);
+
+/*
+ * attn_fwd_ex for the layouts of attn_layout_t.  `max_seqlen` is N for the
+ * fixed-length layouts and, for ATTN_LAYOUT_PACKED, an upper bound on every
+ * sequence length (the work is laid out for it; a tight bound wastes least).
+ * `cu_seqlens` is NULL except for ATTN_LAYOUT_PACKED, where it is a DEVICE
+ * array of B + 1 int32 offsets, 4-byte aligned, non-decreasing, from 0 to
+ * `total_tokens` (the host does not read it; `total_tokens` is ignored for the
+ * other layouts).  Offsets that break these rules are detected on the device:
+ * the offending sequences are skipped (their outputs are not written) and
+ * attn_last_device_error() returns ATTN_ERR_INVALID_ARG.  With
+ * total_tokens == 0 nothing is queued.
+ */
+ATTN_API attn_status_t attn_fwd_layout(const void *q, const void *k, const void *v, void *o, float *lse,
+                              int B, int H, int max_seqlen, int d, float scale, int causal,
+                              attn_dtype_t dtype, attn_layout_t layout, const int *cu_seqlens,
+                              int total_tokens, void *stream);
 
 /*
  * Bytes of device workspace attn_bwd needs: the D vector and L*log2(e)
@@ -100,6 +134,25 @@ ATTN_API attn_status_t attn_bwd_ex(const void *q, const void *k, const void *v, 
                           const void *dout, const float *lse, void *dq, void *dk, void *dv,
                           void *workspace, size_t workspace_bytes, int B, int H, int N, int d,
                           float scale, int causal, attn_dtype_t dtype, void *stream);
+
+/*
+ * Workspace bytes for attn_bwd_layout: three row-indexed arrays as for
+ * attn_bwd_workspace_size, with B H N_pad rows (fixed-length layouts) or
+ * H 128 (ceil(total_tokens / 128) + B) rows (packed: every sequence's rows
+ * start on a 128-row boundary).  0 for arguments it would reject.
+ */
+ATTN_API size_t attn_bwd_layout_workspace_size(int B, int H, int max_seqlen, int d, attn_layout_t layout,
+                                               int total_tokens);
+
+/*
+ * attn_bwd_ex for the layouts of attn_layout_t; the layout arguments as for
+ * attn_fwd_layout, and lse as that call wrote it.
+ */
+ATTN_API attn_status_t attn_bwd_layout(const void *q, const void *k, const void *v, const void *o,
+                              const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                              void *workspace, size_t workspace_bytes, int B, int H, int max_seqlen,
+                              int d, float scale, int causal, attn_dtype_t dtype, attn_layout_t layout,
+                              const int *cu_seqlens, int total_tokens, void *stream);
 
 /*
  * The three kernels attn_bwd_ex queues, one at a time, for callers that time
@@ -157,8 +210,10 @@ ATTN_API const char *attn_status_string(attn_status_t status);
 /*
  * Synchronises `stream`, then reads and clears the device error word of the
  * current device.  Returns ATTN_OK, ATTN_ERR_TIMEOUT (a kernel wait gave up;
- * its outputs are incomplete) or ATTN_ERR_CUDA (the synchronisation failed, or
- * a kernel could not align its shared memory and wrote nothing).
+ * its outputs are incomplete), ATTN_ERR_INVALID_ARG (packed-sequence offsets
+ * that broke the rules of attn_fwd_layout; those sequences were skipped) or
+ * ATTN_ERR_CUDA (the synchronisation failed, or a kernel could not align its
+ * shared memory and wrote nothing).
  */
 ATTN_API attn_status_t attn_last_device_error(void *stream);
 

@@ -70,3 +70,38 @@ def test_argument_checks_before_any_launch(lib):
     assert lib.attn_last_launch_count() == 0
     for s in range(7):
         assert attn.attn_status_string(s).startswith("ATTN_")
+
+
+def test_layout_argument_checks_before_any_launch(lib):
+    import exact_attention_flashattention_gb300 as attn
+    vp = ctypes.c_void_p
+    p = vp(256)  # never dereferenced: every case below is rejected (or has nothing to do) first
+    null = vp(0)
+    cu = vp(4096)
+    BHSD, BSHD, PACKED = 0, 1, 2
+    f = lib.attn_fwd_layout
+    assert f(p, p, p, p, p, 1, 1, 128, 128, 1.0, 1, 0, 7, null, 0, null) == 1         # unknown layout
+    assert f(p, p, p, p, p, 2, 1, 128, 128, 1.0, 1, 0, PACKED, null, 256, null) == 1  # packed needs offsets
+    assert f(p, p, p, p, p, 2, 1, 128, 128, 1.0, 1, 0, BSHD, cu, 256, null) == 1      # offsets only when packed
+    assert f(p, p, p, p, p, 2, 1, 128, 128, 1.0, 1, 0, PACKED, vp(4098), 256, null) == 3  # offsets alignment
+    assert f(p, p, p, p, p, 2, 1, 128, 128, 1.0, 1, 0, PACKED, cu, -1, null) == 1     # negative token count
+    assert f(p, p, p, p, p, 2, 1, 128, 96, 1.0, 1, 0, PACKED, cu, 256, null) == 2     # d unsupported
+    assert f(p, p, p, p, vp(260), 2, 1, 128, 128, 1.0, 1, 0, BSHD, null, 0, null) == 3  # alignment
+    # packed with no tokens at all: nothing to do, nothing queued, no CUDA call
+    assert f(p, p, p, p, p, 2, 1, 128, 128, 1.0, 1, 0, PACKED, cu, 0, null) == 0
+    assert lib.attn_last_launch_count() == 0
+    ws = attn.attn_bwd_layout_workspace_size
+    # fixed-length layouts: the same rows as attn_bwd_workspace_size
+    assert ws(2, 3, 300, 64, "bshd", 0) == attn.attn_bwd_workspace_size(2, 3, 300, 64)
+    assert ws(2, 3, 300, 64, "bhsd", 0) == attn.attn_bwd_workspace_size(2, 3, 300, 64)
+    # packed: per head 128 (ceil(tokens / 128) + B) rows (each sequence padded to whole tiles,
+    # starting on a 128-row boundary)
+    rows = 2 * 128 * (4 + 3)
+    up = lambda x: (x + 255) // 256 * 256
+    lse2 = up(rows * 4)
+    dq = up(lse2 + rows * 4)
+    assert ws(3, 2, 300, 64, "packed", 500) == up(dq + rows * 64 * 4)
+    assert ws(3, 2, 300, 64, "packed", -1) == 0
+    assert lib.attn_bwd_layout(p, p, p, p, p, p, p, p, p, null, 0, 3, 2, 300, 64, 1.0, 1, 0, PACKED, cu, 500,
+                               null) == 4                                            # workspace
+    assert lib.attn_last_launch_count() == 0
