@@ -11,6 +11,8 @@ Names mirror the C ABI:
     attn_fwd_layout(q, k, v, o, lse, scale, causal, layout, cu_seqlens=None, max_seqlen=None, stream=None)
     attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, layout, ...)
     attn_bwd_layout_workspace_size(B, H, max_seqlen, d, layout, total_tokens)
+    attn_decode(q, k_cache, v_cache, o, lse, workspace, scale, cache_seqlens=None, stream=None)
+    attn_decode_workspace_size(B, Hq, Hkv, Nmax, d)
     attn_last_device_error(stream=None)
 plus two allocating conveniences, ``forward`` and ``backward``.
 Tensors are contiguous CUDA tensors of bfloat16 or float16: [B, H, N, d] (layout
@@ -27,7 +29,8 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_stage", "attn_bwd_workspace_size", "attn_last_device_error",
     "attn_status_string", "attn_last_launch_count", "attn_fwd_layout", "attn_bwd_layout",
-    "attn_bwd_layout_workspace_size", "LAYOUTS", "forward", "backward", "library_path", "load",
+    "attn_bwd_layout_workspace_size", "attn_decode", "attn_decode_workspace_size", "LAYOUTS", "forward",
+    "backward", "decode", "library_path", "load",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -42,7 +45,8 @@ LAYOUTS = {"bhsd": 0, "bshd": 1, "packed": 2}
 EXPORTS = (
     "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex", "attn_bwd_stage",
     "attn_status_string", "attn_last_device_error", "attn_last_launch_count", "attn_fwd_layout",
-    "attn_bwd_layout", "attn_bwd_layout_workspace_size", "attn_bwd_noalloc",
+    "attn_bwd_layout", "attn_bwd_layout_workspace_size", "attn_bwd_noalloc", "attn_decode",
+    "attn_decode_workspace_size",
 )
 
 
@@ -79,12 +83,15 @@ def load():
         lib.attn_bwd_layout.argtypes = [vp] * 9 + [vp, sz, i, i, i, i, f, i, i, i, vp, i, vp]
         lib.attn_bwd_layout_workspace_size.argtypes = [i, i, i, i, i, i]
         lib.attn_bwd_layout_workspace_size.restype = sz
+        lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
+        lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
+        lib.attn_decode_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_last_device_error.argtypes = [vp]
         lib.attn_last_launch_count.argtypes = []
         for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_bwd_stage,
-                   lib.attn_fwd_layout, lib.attn_bwd_layout,
+                   lib.attn_fwd_layout, lib.attn_bwd_layout, lib.attn_decode,
                    lib.attn_last_device_error,
                    lib.attn_last_launch_count):
             fn.restype = ctypes.c_int
@@ -210,6 +217,30 @@ def attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, 
         raise AttnError(st, "attn_bwd_layout")
 
 
+def attn_decode_workspace_size(B: int, Hq: int, Hkv: int, Nmax: int, d: int) -> int:
+    return int(load().attn_decode_workspace_size(B, Hq, Hkv, Nmax, d))
+
+
+def attn_decode(q, k_cache, v_cache, o, lse, workspace, scale: float, cache_seqlens=None, stream=None) -> None:
+    """Queue decode attention.  q, o: [B, Hq, d]; k_cache, v_cache: [B, Hkv, Nmax, d];
+    lse: float32 [B, Hq]; cache_seqlens: None or int32 CUDA [B]."""
+    import torch
+    lib = load()
+    B, Hq, d = q.shape
+    _, Hkv, Nmax, _ = k_cache.shape
+    cu = None
+    if cache_seqlens is not None:
+        if cache_seqlens.dtype != torch.int32:
+            raise TypeError("cache_seqlens must be int32")
+        cu = _check(cache_seqlens, "cache_seqlens")
+    st = lib.attn_decode(_check(q, "q"), _check(k_cache, "k_cache"), _check(v_cache, "v_cache"), _check(o, "o"),
+                         _check(lse, "lse"), cu, _check(workspace, "workspace"),
+                         workspace.numel() * workspace.element_size(), B, Hq, Hkv, Nmax, d, float(scale),
+                         _dtype_code(q), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
+
+
 def attn_last_device_error(stream=None) -> int:
     return int(load().attn_last_device_error(_stream_handle(stream)))
 
@@ -253,3 +284,17 @@ def backward(q, k, v, o, dout, lse, scale=None, causal=False, workspace=None, st
         attn_bwd_layout(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale, causal, layout, cu_seqlens, max_seqlen,
                         stream)
     return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, cache_seqlens=None, scale=None, workspace=None, stream=None):
+    """Allocate O, L (and the workspace if not given), queue decode attention, return (O, L)."""
+    import torch
+    B, Hq, d = q.shape
+    _, Hkv, Nmax, _ = k_cache.shape
+    scale = d ** -0.5 if scale is None else scale
+    o = torch.empty_like(q)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = torch.empty(attn_decode_workspace_size(B, Hq, Hkv, Nmax, d), dtype=torch.uint8, device=q.device)
+    attn_decode(q, k_cache, v_cache, o, lse, workspace, scale, cache_seqlens, stream)
+    return o, lse

@@ -157,6 +157,37 @@ WsLayout ws_layout(int B, int H, int N, int d) {
     return ws_layout(s, d);
 }
 
+// Decode work split: chunks of 1024 keys (8 tiles), walked by a persistent grid; a function of
+// the sizes only, so the workspace size needs no device.
+void decode_plan(int B, int Hkv, int Nmax, int& splits, int& chunk) {
+    (void)B;
+    (void)Hkv;
+    chunk = 1024;
+    splits = (Nmax + chunk - 1) / chunk;
+}
+
+attn_status_t check_decode(int B, int Hq, int Hkv, int Nmax, int d) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Nmax <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 128) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)B * Hkv * Nmax * d >= (1ll << 31) || (long long)B * Hq * d >= (1ll << 31)) return ATTN_ERR_UNSUPPORTED;
+    return ATTN_OK;
+}
+
+struct DecodeWs {
+    size_t part_l, total;
+};
+DecodeWs decode_ws(int B, int Hq, int Hkv, int Nmax, int d) {
+    int splits, chunk;
+    decode_plan(B, Hkv, Nmax, splits, chunk);
+    const size_t rows = (size_t)B * Hkv * splits * (Hq / Hkv);
+    DecodeWs w;
+    w.part_l = align_up(rows * d * 4, 256);
+    w.total = align_up(w.part_l + rows * 4, 256);
+    return w;
+}
+
 }  // namespace
 }  // namespace gb300
 
@@ -317,6 +348,55 @@ attn_status_t attn_bwd(const void* q, const void* k, const void* v, const void* 
                        int H, int N, int d, float scale, int causal, void* stream) {
     return attn_bwd_ex(q, k, v, o, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, scale, causal,
                        ATTN_BF16, stream);
+}
+
+size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d) {
+    if (check_decode(B, Hq, Hkv, Nmax, d) != ATTN_OK) return 0;
+    return decode_ws(B, Hq, Hkv, Nmax, d).total;
+}
+
+attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse,
+                          const int* cache_seqlens, void* workspace, size_t workspace_bytes, int B, int Hq, int Hkv,
+                          int Nmax, int d, float scale, attn_dtype_t dtype, void* stream) {
+    t_last_launches = 0;
+    if (!q || !k_cache || !v_cache || !o || !lse) return ATTN_ERR_INVALID_ARG;
+    if (dtype != ATTN_BF16 && dtype != ATTN_FP16) return ATTN_ERR_INVALID_ARG;
+    attn_status_t st = check_decode(B, Hq, Hkv, Nmax, d);
+    if (st != ATTN_OK) return st;
+    const DecodeWs w = decode_ws(B, Hq, Hkv, Nmax, d);
+    if (!workspace || workspace_bytes < w.total) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGNMENT;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_ALIGNMENT;
+    if (cache_seqlens && (reinterpret_cast<uintptr_t>(cache_seqlens) & 3u) != 0) return ATTN_ERR_ALIGNMENT;
+    DevInfo di;
+    if (!dev_info(di)) return ATTN_ERR_CUDA;
+    DecodeArgs a;
+    std::memset(&a, 0, sizeof(a));
+    const int G = Hq / Hkv;
+    if (!make_map(&a.tm_q, q, B * Hkv, G, d) || !make_map(&a.tm_k, k_cache, B * Hkv, Nmax, d) ||
+        !make_map(&a.tm_v, v_cache, B * Hkv, Nmax, d))
+        return ATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.seqlens = cache_seqlens;
+    a.part_o = reinterpret_cast<float*>(ws);
+    a.part_l = reinterpret_cast<float*>(ws + w.part_l);
+    a.o = o;
+    a.lse = lse;
+    a.groups = B * Hkv;
+    a.Hkv = Hkv;
+    a.G = G;
+    a.Nmax = Nmax;
+    a.d = d;
+    decode_plan(B, Hkv, Nmax, a.splits, a.chunk);
+    a.scale = scale;
+    a.fp16 = dtype == ATTN_FP16;
+    a.stage = -1;
+    a.num_sms = di.sms;
+    a.error = di.err_ptr;
+    if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_launches = 2;
+    return ATTN_OK;
 }
 
 const char* attn_status_string(attn_status_t s) {

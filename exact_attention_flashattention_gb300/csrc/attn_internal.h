@@ -69,7 +69,27 @@ struct BwdArgs {
     int* error;
 };
 
+// Decode: one query row per head against a [B, Hkv, Nmax, d] key/value cache (decode.cu).
+struct DecodeArgs {
+    CUtensorMap tm_q;        // q [B, Hq, d] viewed as [B Hkv, G, d]; box rows past G are zero-filled
+    CUtensorMap tm_k, tm_v;  // caches [B Hkv, Nmax, d]
+    const int* seqlens;      // device [B] cache lengths, or nullptr (every batch Nmax)
+    float* part_o;           // workspace [B Hkv, splits, G, d]: each chunk's normalised O
+    float* part_l;           // workspace [B Hkv, splits, G]: each chunk's L (natural log)
+    void* o;                 // [B, Hq, d] 16-bit
+    float* lse;              // [B, Hq]
+    int groups;              // B Hkv
+    int Hkv, G, Nmax, d;
+    int splits, chunk;       // key chunks per group, keys per chunk (multiple of 128)
+    float scale;
+    int fp16;
+    int stage;               // -1 both kernels, 0 the chunk kernel, 1 the combination
+    int num_sms;
+    int* error;
+};
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // stage: -1 = all three kernels; 0 = preprocess; 1 = main kernel; 2 = dQ conversion.
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage);
 

@@ -204,6 +204,35 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void *q, const void *k, const void
                                void *dk, void *dv, int B, int H, int N, int d, float scale,
                                int causal, attn_dtype_t dtype, void *stream);
 
+/*
+ * Decode: attention of one new query per head against a key/value cache (the
+ * forward equations with a single query row and no mask; the
+ * flash_attention_cuda README leaves this "different, memory-bound problem"
+ * out).  For batch b and query head h, with G = Hq / Hkv query heads sharing
+ * KV head h / G (grouped-query attention; G = 1 is plain multi-head):
+ *   o[b, h, :] = softmax(scale q[b, h, :] K_b^T) V_b,
+ *   lse[b, h]  = log sum_j exp(scale q[b, h, :] . K_b[j, :])
+ * over the cached keys j < len_b of K_b = k_cache[b, h / G], V_b likewise.
+ *   q, o        [B, Hq, d] 16-bit;  lse [B, Hq] FP32 (natural log)
+ *   k_cache,
+ *   v_cache     [B, Hkv, Nmax, d] 16-bit
+ *   cache_seqlens  NULL (every len_b = Nmax) or a DEVICE int32 array [B],
+ *               4-byte aligned, each 0 <= len_b <= Nmax.  A length outside
+ *               that range is treated as 0 and attn_last_device_error()
+ *               returns ATTN_ERR_INVALID_ARG; len_b = 0 gives o = 0 and
+ *               lse = -inf.
+ * Requires Hq a multiple of Hkv, G <= 128, d in {64, 128}, the sizes of the
+ * other calls' limits, and a caller-owned `workspace` of at least
+ * attn_decode_workspace_size() bytes, 256-byte aligned (the keys are split
+ * into chunks processed in parallel; the workspace holds each chunk's partial
+ * result).  Queues two kernels.
+ */
+ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d);
+ATTN_API attn_status_t attn_decode(const void *q, const void *k_cache, const void *v_cache, void *o,
+                          float *lse, const int *cache_seqlens, void *workspace,
+                          size_t workspace_bytes, int B, int Hq, int Hkv, int Nmax, int d,
+                          float scale, attn_dtype_t dtype, void *stream);
+
 /* Static string naming a status code. */
 ATTN_API const char *attn_status_string(attn_status_t status);
 

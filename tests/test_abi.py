@@ -105,3 +105,29 @@ def test_layout_argument_checks_before_any_launch(lib):
     assert lib.attn_bwd_layout(p, p, p, p, p, p, p, p, p, null, 0, 3, 2, 300, 64, 1.0, 1, 0, PACKED, cu, 500,
                                null) == 4                                            # workspace
     assert lib.attn_last_launch_count() == 0
+
+
+def test_decode_argument_checks_before_any_launch(lib):
+    import exact_attention_flashattention_gb300 as attn
+    vp = ctypes.c_void_p
+    p = vp(256)
+    null = vp(0)
+    d = lib.attn_decode
+    wsz = attn.attn_decode_workspace_size
+    # chunks of 1024 keys; per (group, chunk, query head): d FP32 values and one L
+    rows = 2 * 2 * 3 * 4                    # B Hkv, 3 chunks of 3000 keys, G = 4
+    up = lambda x: (x + 255) // 256 * 256
+    assert wsz(2, 8, 2, 3000, 128) == up(up(rows * 128 * 4) + rows * 4)
+    assert wsz(2, 6, 4, 3000, 128) == 0      # Hq not a multiple of Hkv
+    assert wsz(1, 256, 1, 100, 64) == 0      # G > 128
+    assert wsz(1, 4, 4, 100, 96) == 0        # d unsupported
+    n = wsz(2, 8, 2, 1000, 128)
+    assert d(null, p, p, p, p, null, p, n, 2, 8, 2, 1000, 128, 1.0, 0, null) == 1          # null q
+    assert d(p, p, p, p, p, null, p, n, 2, 6, 4, 1000, 128, 1.0, 0, null) == 1             # Hq % Hkv
+    assert d(p, p, p, p, p, null, p, n, 2, 8, 2, 1000, 96, 1.0, 0, null) == 2              # d unsupported
+    assert d(p, p, p, p, p, null, null, 0, 2, 8, 2, 1000, 128, 1.0, 0, null) == 4          # workspace
+    assert d(p, p, p, p, p, null, vp(512), n - 1, 2, 8, 2, 1000, 128, 1.0, 0, null) == 4   # too small
+    assert d(p, p, p, p, p, null, vp(512 + 16), n, 2, 8, 2, 1000, 128, 1.0, 0, null) == 3  # ws alignment
+    assert d(p, p, p, p, p, vp(258), p, n, 2, 8, 2, 1000, 128, 1.0, 0, null) == 3          # lengths alignment
+    assert d(p, p, p, p, p, null, p, n, 2, 8, 2, 1000, 128, 1.0, 5, null) == 1             # bad dtype
+    assert lib.attn_last_launch_count() == 0
