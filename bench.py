@@ -429,6 +429,15 @@ SWEEP = [
 ]
 
 
+# Decode (one query per head against a key/value cache): name, B, Hq, Hkv, cache length, d.
+DECODE_SWEEP = [
+    ("decode GQA B=8 Hq=32 Hkv=8 N=32768 d=128", 8, 32, 8, 32768, 128),
+    ("decode MHA B=32 H=32 N=4096 d=128", 32, 32, 32, 4096, 128),
+    ("decode GQA B=1 Hq=32 Hkv=8 N=131072 d=128", 1, 32, 8, 131072, 128),
+    ("decode MHA B=64 H=16 N=2048 d=64", 64, 16, 16, 2048, 64),
+]
+
+
 def run_sweep(iters=20):
     """Forward and backward TFLOPS of every workload of the list (CUDA events,
     3 warm-up calls, `iters` timed calls each).  One JSON line per workload;
@@ -476,6 +485,38 @@ def run_sweep(iters=20):
                           "fwd_pct_peak": 100 * ftf / burst, "bwd_ms": bms, "bwd_tflops": btf,
                           "bwd_pct_peak": 100 * btf / burst, "peak_basis": f"bf16 burst {burst} ({src})"}),
               flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+    # decode against a key/value cache: HBM-bound, reported in GB/s of the cache bytes read
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    for name, B, Hq, Hkv, N, d in DECODE_SWEEP:
+        g = torch.Generator(device=dev)
+        g.manual_seed(11)
+        q = torch.randn((B, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+        kc, vc = (torch.randn((B, Hkv, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
+        o, lse = torch.empty_like(q), torch.empty((B, Hq), device=dev)
+        ws = torch.empty(attn.attn_decode_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+
+        def timed_dec():
+            for _ in range(3):
+                attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(iters):
+                attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / iters
+
+        ms = timed_dec()
+        if attn.attn_last_device_error(stream) != 0:
+            raise RuntimeError("device error word set")
+        cache_bytes = 2 * B * Hkv * N * d * 2          # K and V, each read once
+        gbs = cache_bytes / ms / 1e6
+        print(json.dumps({"sweep": name, "dtype": "bf16", "decode_us": 1e3 * ms, "cache_gb": cache_bytes / 1e9,
+                          "gbs": gbs, "pct_hbm": 100 * gbs / hbm, "peak_basis": f"HBM copy {hbm} GB/s ({src})"}),
+              flush=True)
+        del q, kc, vc, o, lse, ws
     return 0
 
 

@@ -47,11 +47,11 @@ struct DecLayout {
     static constexpr int kTile = 128 * D * 2;
     static constexpr int kPanels = D / 64;
     static constexpr int kStages = D == 128 ? 4 : 8;  // 128 KB of K/V tiles in flight either way
-    static constexpr int kQ = 0;
-    static constexpr int kKV = kTile;
+    static constexpr int kQ = 0;          // [2]: non-empty item i uses slot i % 2, so the next
+    static constexpr int kKV = 2 * kTile;  // item's Q loads while this one runs
     static constexpr int kAux = kKV + kStages * kTile;
-    static constexpr int kBarQFull = 0, kBarQEmpty = 1;
-    static constexpr int kBarKVFull = 2;
+    static constexpr int kBarQFull = 0, kBarQEmpty = 2;  // [2] each
+    static constexpr int kBarKVFull = 4;
     static constexpr int kBarKVEmpty = kBarKVFull + kStages;
     static constexpr int kBarSFull = kBarKVEmpty + kStages;  // [2]: tile g uses buffer g % 2
     static constexpr int kBarPReady = kBarSFull + 2;         // [2]
@@ -106,8 +106,10 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const int active_warps = min(4, (G + 31) / 32);  // softmax warps holding at least one real row
 
     if (threadIdx.x == 0) {
-        mbar_init(&bars[L::kBarQFull], 1);
-        mbar_init(&bars[L::kBarQEmpty], 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&bars[L::kBarQFull + q], 1);
+            mbar_init(&bars[L::kBarQEmpty + q], 1);
+        }
         for (int st = 0; st < L::kStages; ++st) {
             mbar_init(&bars[L::kBarKVFull + st], 1);
             mbar_init(&bars[L::kBarKVEmpty + st], 1);
@@ -273,7 +275,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // ------------------------------------------------------------ MMA issuer (whole warp)
         constexpr uint32_t kIdescQK = idesc_f16(128, 128, BF16, false, false);
         constexpr uint32_t kIdescPV = idesc_f16(128, D, BF16, false, true);
-        const uint32_t q_base = smem_u32(smem + L::kQ);
+        const uint32_t q_base0 = smem_u32(smem + L::kQ);
+        uint32_t q_base = q_base0;
         const uint32_t kv_base = smem_u32(smem + L::kKV);
         bool ok = true;
         // The ring's tokens are K(0) V(0) K(1) V(1) ... over the global tile index g: K(g) is token
@@ -305,8 +308,9 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             DecItem w;
             dec_item(u, splits, chunk, Hkv, Nmax, seqlens, error, false, w);
             if (w.n_tiles == 0) continue;
-            if (!warp_mbar_wait(&bars[L::kBarQFull], qi & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+            if (!warp_mbar_wait(&bars[L::kBarQFull + (qi & 1)], (qi >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
             tc_fence_after();
+            q_base = q_base0 + (qi & 1) * L::kTile;
             for (int j = 0; j <= w.n_tiles && ok; ++j) {
                 // S(g) into buffer g % 2 as soon as K(g) is in (the buffer's previous contents,
                 // P(g-2), were read by PV(g-2), issued earlier), then PV(g-1) once P(g-1) and
@@ -332,7 +336,7 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 }
             }
             if (!ok) break;
-            warp_mma_commit(&bars[L::kBarQEmpty]);  // every MMA that read this Q has been issued
+            warp_mma_commit(&bars[L::kBarQEmpty + (qi & 1)]);  // every MMA that reads this Q slot is issued
             gt += w.n_tiles;
             ++qi;
         }
@@ -346,11 +350,16 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             DecItem w;
             dec_item(u, splits, chunk, Hkv, Nmax, seqlens, error, false, w);
             if (w.n_tiles == 0) continue;
-            if (qi > 0 && !mbar_wait(&bars[L::kBarQEmpty], (qi - 1) & 1, guard, kDevTimeoutLoad)) { ok = false; break; }
-            mbar_arrive_expect_tx(&bars[L::kBarQFull], L::kTile);
+            const uint32_t qs = qi & 1;
+            if (qi >= 2 && !mbar_wait(&bars[L::kBarQEmpty + qs], ((qi >> 1) - 1) & 1, guard, kDevTimeoutLoad)) {
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&bars[L::kBarQFull + qs], L::kTile);
 #pragma unroll
             for (int p = 0; p < L::kPanels; ++p)
-                tma_load_3d(smem + L::kQ + p * kPanelBytes, &tm_q, &bars[L::kBarQFull], 64 * p, 0, w.bh);
+                tma_load_3d(smem + L::kQ + qs * L::kTile + p * kPanelBytes, &tm_q, &bars[L::kBarQFull + qs], 64 * p, 0,
+                            w.bh);
             ++qi;
             for (int j = 0; j < w.n_tiles && ok; ++j) {
 #pragma unroll
@@ -372,7 +381,8 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
             }
         }
         // Let every copy issued above land before shared memory is released.
-        if (qi > 0) mbar_wait_drain(&bars[L::kBarQFull], (qi - 1) & 1, kWaitLimitNs);
+        for (uint32_t i = (qi > 2 ? qi - 2 : 0); i < qi; ++i)
+            mbar_wait_drain(&bars[L::kBarQFull + (i & 1)], (i >> 1) & 1, kWaitLimitNs);
         for (uint32_t t = (tok > (uint32_t)L::kStages ? tok - L::kStages : 0); t < tok; ++t)
             mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
     }
