@@ -486,37 +486,47 @@ def run_sweep(iters=20):
                           "bwd_pct_peak": 100 * btf / burst, "peak_basis": f"bf16 burst {burst} ({src})"}),
               flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
-    # decode against a key/value cache: HBM-bound, reported in GB/s of the cache bytes read
-    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     for name, B, Hq, Hkv, N, d in DECODE_SWEEP:
-        g = torch.Generator(device=dev)
-        g.manual_seed(11)
-        q = torch.randn((B, Hq, d), generator=g, device=dev).to(torch.bfloat16)
-        kc, vc = (torch.randn((B, Hkv, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
-        o, lse = torch.empty_like(q), torch.empty((B, Hq), device=dev)
-        ws = torch.empty(attn.attn_decode_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+        run_decode(name, B, Hq, Hkv, N, d, iters=iters, warmup=3, build=False)
+    return 0
 
-        def timed_dec():
-            for _ in range(3):
-                attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            a.record(stream)
-            for _ in range(iters):
-                attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            return a.elapsed_time(b) / iters
 
-        ms = timed_dec()
-        if attn.attn_last_device_error(stream) != 0:
-            raise RuntimeError("device error word set")
-        cache_bytes = 2 * B * Hkv * N * d * 2          # K and V, each read once
-        gbs = cache_bytes / ms / 1e6
-        print(json.dumps({"sweep": name, "dtype": "bf16", "decode_us": 1e3 * ms, "cache_gb": cache_bytes / 1e9,
-                          "gbs": gbs, "pct_hbm": 100 * gbs / hbm, "peak_basis": f"HBM copy {hbm} GB/s ({src})"}),
-              flush=True)
-        del q, kc, vc, o, lse, ws
+def run_decode(name, B, Hq, Hkv, N, d, iters=20, warmup=3, build=True):
+    """Decode against a key/value cache: HBM-bound, reported in GB/s of the cache bytes read
+    (CUDA events, `warmup` untimed and `iters` timed calls of attn_decode).  One JSON line."""
+    import torch
+
+    if build:
+        import __graft_entry__
+        __graft_entry__.build()
+    import exact_attention_flashattention_gb300 as attn
+    peaks, src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    q = torch.randn((B, Hq, d), generator=g, device=dev).to(torch.bfloat16)
+    kc, vc = (torch.randn((B, Hkv, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
+    o, lse = torch.empty_like(q), torch.empty((B, Hq), device=dev)
+    ws = torch.empty(attn.attn_decode_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(iters):
+        attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / iters
+    if attn.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set")
+    cache_bytes = 2 * B * Hkv * N * d * 2          # K and V, each read once
+    gbs = cache_bytes / ms / 1e6
+    print(json.dumps({"sweep": name, "dtype": "bf16", "decode_us": 1e3 * ms, "cache_gb": cache_bytes / 1e9,
+                      "gbs": gbs, "pct_hbm": 100 * gbs / hbm, "peak_basis": f"HBM copy {hbm} GB/s ({src})"}),
+          flush=True)
     return 0
 
 
@@ -532,6 +542,8 @@ def main():
                     help="print fwd / bwd TFLOPS of every workload of the list instead of the bench line")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,d[,noncausal] instead of the default workload (smaller cases for profiling)")
+    ap.add_argument("--decode-shape", default=None,
+                    help="B,Hq,Hkv,N,d: time decode on that cache (--steps timed calls, --warmup untimed)")
     args = ap.parse_args()
     if args.shape:
         parts = args.shape.split(",")
@@ -544,6 +556,10 @@ def main():
         args.warmup = 3
     if args.sweep:
         return run_sweep()
+    if args.decode_shape:
+        B, Hq, Hkv, N, d = (int(x) for x in args.decode_shape.split(","))
+        return run_decode(f"decode B={B} Hq={Hq} Hkv={Hkv} N={N} d={d}", B, Hq, Hkv, N, d, iters=args.steps,
+                          warmup=args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
