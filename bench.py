@@ -486,6 +486,52 @@ def run_sweep(iters=20):
                           "bwd_pct_peak": 100 * btf / burst, "peak_basis": f"bf16 burst {burst} ({src})"}),
               flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
+    # the same causal d = 128 work in the token-major layouts: BSHD, and 32 packed sequences of
+    # lengths 512, 752, ..., 7952 (135424 tokens; most not a multiple of 128)
+    lens = [512 + 240 * i for i in range(32)]
+    for name, layout in (("layout BSHD causal B=8 H=16 N=4096 d=128", "bshd"),
+                         (f"layout packed causal 32 sequences, {sum(lens)} tokens, H=16 d=128", "packed")):
+        H, d = 16, 128
+        if layout == "bshd":
+            B, N = 8, 4096
+            shape, cu, total, maxlen = (B, N, H, d), None, B * N, N
+            flop_f, flop_b = F.fwd_flops(B, H, N, d, True), F.bwd_flops(B, H, N, d, True)
+        else:
+            B, total, maxlen = len(lens), sum(lens), max(lens)
+            shape = (total, H, d)
+            cu = torch.tensor([0] + list(torch.tensor(lens).cumsum(0)), dtype=torch.int32, device=dev)
+            flop_f = sum(F.fwd_flops(1, H, n, d, True) for n in lens)
+            flop_b = sum(F.bwd_flops(1, H, n, d, True) for n in lens)
+        g = torch.Generator(device=dev)
+        g.manual_seed(13)
+        q, k, v, do = (torch.randn(shape, generator=g, device=dev).to(torch.bfloat16) for _ in range(4))
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, N) if layout == "bshd" else (H, total), device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws = torch.empty(attn.attn_bwd_layout_workspace_size(B, H, maxlen, d, layout, total), dtype=torch.uint8,
+                         device=dev)
+        sc = d ** -0.5
+
+        def timed_l(fn):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            for _ in range(iters):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            return a.elapsed_time(b) / iters
+
+        fms = timed_l(lambda: attn.attn_fwd_layout(q, k, v, o, lse, sc, True, layout, cu, maxlen, stream))
+        bms = timed_l(lambda: attn.attn_bwd_layout(q, k, v, o, do, lse, dq, dk, dv, ws, sc, True, layout, cu, maxlen,
+                                                   stream))
+        if attn.attn_last_device_error(stream) != 0:
+            raise RuntimeError("device error word set")
+        print(json.dumps({"sweep": name, "dtype": "bf16", "fwd_ms": fms, "fwd_tflops": flop_f / fms / 1e9,
+                          "bwd_ms": bms, "bwd_tflops": flop_b / bms / 1e9}), flush=True)
+        del q, k, v, do, o, lse, dq, dk, dv, ws
     for name, B, Hq, Hkv, N, d in DECODE_SWEEP:
         run_decode(name, B, Hq, Hkv, N, d, iters=iters, warmup=3, build=False)
     return 0

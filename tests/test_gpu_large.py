@@ -136,3 +136,43 @@ def test_full_size_against_oracle(attn, cid, B, H, N, d, causal, dtype, sigma):
             assert e <= TOL_GRAD_RELFRO, (name, "whole head", e)
             worst["dkdv_tail"] = max(worst["dkdv_tail"], e)
     print(f"\n{cid}: worst O {worst['o']:.4g} L {worst['l']:.3g} dQ-rows {worst['dq']:.3g} dK/dV {worst['dkdv_tail']:.3g}")
+
+
+def test_largest_supported_size(attn):
+    """B H N_pad d just below 2^31 elements, the documented limit: every kernel's 64-bit
+    offsets.  131071 heads of N = 128, d = 128 (4.3 GB per tensor).  Every head is checked
+    on the device (finite outputs, sum_j dK_j = 0); sampled heads, whose inputs come from the
+    seeded generator, against the oracle."""
+    B, H, N, d, causal, dtype = 1, 131071, 128, 128, True, "bf16"
+    assert B * H * N * d < 2 ** 31
+    scale = 1.0 / math.sqrt(d)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(99)
+    heads = [0, 1, 65535, H - 2, H - 1]
+    x = {n: si.tensor_heads(SEED, n, B * H, N, d, 1.0, dtype, heads=heads) for n in ("q", "k", "v", "do")}
+    t = {}
+    for n in ("q", "k", "v", "do"):
+        t[n] = torch.randn((B, H, N, d), generator=gen, device="cuda", dtype=torch.float32).to(torch.bfloat16)
+        for idx, h in enumerate(heads):
+            t[n][0, h] = torch.from_numpy(np.ascontiguousarray(x[n][idx]).view(np.int16)).to("cuda").view(torch.bfloat16)
+    o = torch.full_like(t["q"], float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    attn.attn_fwd(t["q"], t["k"], t["v"], o, lse, scale, causal)
+    dq, dk, dv = (torch.full_like(t["q"], float("nan")) for _ in range(3))
+    ws = torch.empty(attn.attn_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    attn.attn_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, dq, dk, dv, ws, scale, causal)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+    del ws
+    for name, tt in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+        assert bool(torch.isfinite(tt).all()), f"{name}: unwritten or non-finite elements"
+    colsum = dk.float().sum(dim=2).abs()
+    colabs = dk.float().abs().sum(dim=2) + 1e-6
+    assert float((colsum / colabs).max()) < 2e-2, "sum_j dK_j != 0"
+    for idx, h in enumerate(heads):
+        ref = oracle.attn_bwd(*(si.bits_to_f32(x[n][idx], dtype).astype(np.float64) for n in ("q", "k", "v", "do")),
+                              scale, causal)
+        assert np.max(np.abs(to_f64(o[0, h]) - ref["o"])) <= o_tolerance(ref["o"], dtype).max(), h
+        assert np.max(np.abs(to_f64(lse[0, h]) - ref["lse"])) <= TOL_L_MAXABS, h
+        for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+            assert rel_fro(to_f64(got[0, h]), ref[name]) <= TOL_GRAD_RELFRO, (h, name)
