@@ -157,12 +157,11 @@ WsLayout ws_layout(int B, int H, int N, int d) {
     return ws_layout(s, d);
 }
 
-// Decode work split: chunks of 1024 keys (8 tiles), walked by a persistent grid; a function of
-// the sizes only, so the workspace size needs no device.
-void decode_plan(int B, int Hkv, int Nmax, int& splits, int& chunk) {
-    (void)B;
-    (void)Hkv;
-    chunk = 1024;
+// Decode work split: chunks of 512 KB of K / V (1024 keys at d = 128, 2048 at d = 64, eight or
+// sixteen 128-key tiles), walked by a persistent grid; a function of the sizes only, so the
+// workspace size needs no device.
+void decode_plan(int Nmax, int d, int& splits, int& chunk) {
+    chunk = d == 128 ? 1024 : 2048;
     splits = (Nmax + chunk - 1) / chunk;
 }
 
@@ -180,7 +179,7 @@ struct DecodeWs {
 };
 DecodeWs decode_ws(int B, int Hq, int Hkv, int Nmax, int d) {
     int splits, chunk;
-    decode_plan(B, Hkv, Nmax, splits, chunk);
+    decode_plan(Nmax, d, splits, chunk);
     const size_t rows = (size_t)B * Hkv * splits * (Hq / Hkv);
     DecodeWs w;
     w.part_l = align_up(rows * d * 4, 256);
@@ -388,7 +387,7 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     a.G = G;
     a.Nmax = Nmax;
     a.d = d;
-    decode_plan(B, Hkv, Nmax, a.splits, a.chunk);
+    decode_plan(Nmax, d, a.splits, a.chunk);
     a.scale = scale;
     a.fp16 = dtype == ATTN_FP16;
     a.stage = -1;

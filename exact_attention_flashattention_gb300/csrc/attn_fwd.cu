@@ -398,6 +398,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 issue_qk(1, kslot);
                 warp_mma_commit(&bars[L::kBarSFull + 1]);
                 warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                // Q is read by the S MMAs only: the Q buffers are released after the item's last
+                // S (S_1(n1 - 1); S_0's last comes no later), so that the next item's Q loads
+                // while this item's last PVs and epilogue run.
+                if (w.n1 == 1) warp_mma_commit(&bars[L::kBarQEmpty]);
                 for (int j = 0; j < w.n1 && ok; ++j) {
                     uint32_t vslot;
                     if (!wait_kv(vslot)) { ok = false; break; }
@@ -418,13 +422,13 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             }
                             issue_qk(q, kslot);
                             warp_mma_commit(&bars[L::kBarSFull + q]);
+                            if (q == 1 && j + 2 == w.n1) warp_mma_commit(&bars[L::kBarQEmpty]);
                         }
                     }
                     if (!ok) break;
                     warp_mma_commit(&bars[L::kBarKVEmpty + vslot]);
                     if (have_k) warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
                 }
-                warp_mma_commit(&bars[L::kBarQEmpty]);
             }
             // Every MMA issued above completes before TMEM is released.
             warp_mma_commit(&bars[L::kBarTeardown]);

@@ -14,7 +14,8 @@
 //    (b, hkv) are the rows of one zero-padded 128-row Q tile, so one
 //    S = Q K^T MMA (tcgen05, M = 128) serves all of them and K / V are read
 //    once per group;
-//  * split KV: the keys of a group are cut into chunks of 1024, and a
+//  * split KV: the keys of a group are cut into chunks of 512 KB of K / V
+//    (1024 keys at d = 128, 2048 at d = 64), and a
 //    persistent grid (one CTA per SM) walks the (group, chunk) items, so that
 //    even a small batch covers every SM with little tail; each item writes its
 //    chunk's O (normalised) and L, and a second kernel combines the chunks:
@@ -395,41 +396,80 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     }
 }
 
-// o[b, hkv G + r, :] and L from the chunks' partial results (one warp per query head).
+// o[b, hkv G + r, :] and L from the chunks' partial results: one CTA of 512 threads per query
+// head.  All threads first reduce the chunks' L to their maximum and the weight sum; then thread
+// t adds column t % d of the chunks s = t / d, t / d + 512 / d, ... (coalesced rows of the
+// partial O, several loads in flight per thread), and the 512 / d partial sums are added in
+// shared memory.  Chunk counts reach the hundreds for long caches, so the chunks are spread
+// over threads rather than walked by one warp.
+constexpr int kCombThreads = 512;
+
 template <int D, bool BF16>
-__global__ void __launch_bounds__(256) attn_decode_combine_kernel(const float* __restrict__ part_o,
-                                                                  const float* __restrict__ part_l,
-                                                                  void* __restrict__ o, float* __restrict__ lse,
-                                                                  int n_rows, int G, int splits) {
-    const int gw = (int)((blockIdx.x * (size_t)blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (gw >= n_rows) return;
-    const int bh = gw / G, r = gw - bh * G;  // query head b Hq + hkv G + r == gw
-    float lmax = -INFINITY;
-    for (int s = 0; s < splits; ++s) lmax = fmaxf(lmax, part_l[((size_t)bh * splits + s) * G + r]);
-    constexpr int PER = D / 32;  // values per lane
-    float acc[PER];
+__global__ void __launch_bounds__(kCombThreads) attn_decode_combine_kernel(const float* __restrict__ part_o,
+                                                                           const float* __restrict__ part_l,
+                                                                           void* __restrict__ o, float* __restrict__ lse,
+                                                                           int G, int splits) {
+    constexpr int kGroups = kCombThreads / D;
+    __shared__ float red[kCombThreads / 32];
+    __shared__ float part[kGroups][D];
+    const int row = blockIdx.x;  // query head b Hq + hkv G + r
+    const int bh = row / G, r = row - bh * G;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float* pl = part_l + (size_t)bh * splits * G + r;  // chunk s at pl[s * G]
+
+    float m = -INFINITY;
+    for (int s = tid; s < splits; s += kCombThreads) m = fmaxf(m, pl[(size_t)s * G]);
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    float lmax = red[0];
+#pragma unroll
+    for (int w = 1; w < kCombThreads / 32; ++w) lmax = fmaxf(lmax, red[w]);
+    __syncthreads();
+
+    float ws = 0.f;
+    if (lmax != -INFINITY)
+        for (int s = tid; s < splits; s += kCombThreads) ws += __expf(pl[(size_t)s * G] - lmax);  // 0 when empty
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+    if (lane == 0) red[warp] = ws;
+    __syncthreads();
     float wsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < kCombThreads / 32; ++w) wsum += red[w];
+
+    const int e = tid % D, grp = tid / D;
+    float acc = 0.f;
     if (lmax != -INFINITY) {
-        for (int s = 0; s < splits; ++s) {
-            const float ls = part_l[((size_t)bh * splits + s) * G + r];
-            const float wgt = __expf(ls - lmax);  // 0 for an empty chunk
-            wsum += wgt;
-            const float* src = part_o + (((size_t)bh * splits + s) * G + r) * D + lane * PER;
+        const float* po = part_o + ((size_t)bh * splits * G + r) * D + e;  // chunk s at po[s * G * D]
+        int s = grp;
+        for (; s + 3 * kGroups < splits; s += 4 * kGroups) {
+            float l4[4], v4[4];
 #pragma unroll
-            for (int e = 0; e < PER; ++e) acc[e] += wgt * src[e];
+            for (int u = 0; u < 4; ++u) {
+                l4[u] = pl[(size_t)(s + u * kGroups) * G];
+                v4[u] = po[(size_t)(s + u * kGroups) * G * D];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) acc += __expf(l4[u] - lmax) * v4[u];
         }
+        for (; s < splits; s += kGroups) acc += __expf(pl[(size_t)s * G] - lmax) * po[(size_t)s * G * D];
     }
-    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-    uint32_t pk[PER / 2];
+    part[grp][e] = acc;
+    __syncthreads();
+    if (tid < D) {
+        float t = 0.f;
 #pragma unroll
-    for (int e = 0; e < PER / 2; ++e) pk[e] = pack2<BF16>(acc[2 * e] * inv, acc[2 * e + 1] * inv);
-    uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(o) + ((size_t)gw * D + lane * PER) * 2);
-#pragma unroll
-    for (int e = 0; e < PER / 2; ++e) dst[e] = pk[e];
-    if (lane == 0) lse[gw] = lmax == -INFINITY ? -INFINITY : lmax + logf(wsum);
+        for (int g = 0; g < kGroups; ++g) t += part[g][tid];
+        part[0][tid] = wsum > 0.f ? t / wsum : 0.f;
+    }
+    __syncthreads();
+    if (tid < D / 2) {
+        uint32_t* dst = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(o) + (size_t)row * D * 2);
+        dst[tid] = pack2<BF16>(part[0][2 * tid], part[0][2 * tid + 1]);
+    }
+    if (tid == 0) lse[row] = lmax == -INFINITY ? -INFINITY : lmax + logf(wsum);
 }
 
 template <int D, bool BF16>
@@ -450,9 +490,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
     }
     if (a.stage < 0 || a.stage == 1) {
         const long rows = (long)a.groups * a.G;
-        const long blocks = (rows * 32 + 255) / 256;
-        attn_decode_combine_kernel<D, BF16><<<(unsigned)blocks, 256, 0, stream>>>(a.part_o, a.part_l, a.o, a.lse,
-                                                                                 (int)rows, a.G, a.splits);
+        attn_decode_combine_kernel<D, BF16><<<(unsigned)rows, kCombThreads, 0, stream>>>(a.part_o, a.part_l, a.o,
+                                                                                         a.lse, a.G, a.splits);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -5,7 +5,7 @@ the row of a query matrix whose row 0 is q[b, h] over the cache's first len_b
 keys, non-causal (every cached key is visible), which is the decode output.
 Cases cover grouped queries (G = Hq / Hkv from 1 to 128, i.e. one to all four
 softmax warps), d = 64 and 128, bf16 and fp16, cache lengths of 0, 1, ragged and
-full, several 1024-key chunks, and more work items than SMs.  Tolerances as for
+full, several key chunks (1024 keys at d = 128, 2048 at d = 64), and more work items than SMs.  Tolerances as for
 the forward: O max-abs 1e-2, L max-abs 1e-3.  Outputs are pre-filled with NaN.
 """
 import math
@@ -29,6 +29,7 @@ CASES = [
     (1, 64, 1, 300, 64, "bf16", None),
     (1, 128, 1, 200, 128, "bf16", None),
     (16, 32, 8, 3000, 128, "bf16", None),      # 128 groups x 3 chunks: more items than SMs
+    (2, 8, 4, 5000, 64, "fp16", [5000, 2049]),  # d = 64: three 2048-key chunks, one of them a single key
 ]
 
 
