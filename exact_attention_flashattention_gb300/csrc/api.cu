@@ -1,5 +1,6 @@
 // C-ABI entry points of libattn_gb300.so: argument checks, tensor-map
 // encoding, workspace carving and kernel dispatch.  Declared in include/attn.h.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -11,6 +12,13 @@ namespace gb300 {
 
 // Device error word written by kernels whose bounded waits gave up.
 __device__ int g_device_error = 0;
+
+// Work counters of the persistent kernels' dynamic unit distribution: each launch takes the
+// next slot (round robin) and zeroes it on its stream before the kernel runs, so launches in
+// flight at the same time (other streams, or graph replays) use different counters as long as
+// fewer than kSchedSlots of them overlap.
+constexpr int kSchedSlots = 1024;
+__device__ unsigned int g_sched_counters[kSchedSlots];
 
 namespace {
 
@@ -38,6 +46,7 @@ struct DevInfo {
     int device = 0;
     int sms = 0;
     int* err_ptr = nullptr;
+    unsigned int* sched_base = nullptr;
 };
 
 // Per-device cache of the SM count and of the device address of the error word.
@@ -53,6 +62,8 @@ bool dev_info(DevInfo& out) {
         di.device = dev;
         if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         if (cudaGetSymbolAddress(reinterpret_cast<void**>(&di.err_ptr), g_device_error) != cudaSuccess) return false;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&di.sched_base), g_sched_counters) != cudaSuccess)
+            return false;
         cache[dev] = di;
         have[dev] = true;
     }
@@ -94,6 +105,14 @@ bool make_map_seq(CUtensorMap* m, const void* base, const SeqDesc& s, int d) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A zeroed work counter for one launch on `stream` (nullptr if the memset could not be queued).
+unsigned int* take_sched_counter(const DevInfo& di, cudaStream_t stream) {
+    static std::atomic<unsigned int> next{0};
+    unsigned int* p = di.sched_base + (next.fetch_add(1, std::memory_order_relaxed) % kSchedSlots);
+    if (cudaMemsetAsync(p, 0, sizeof(unsigned int), stream) != cudaSuccess) return nullptr;
+    return p;
+}
 
 size_t n_pad_of(int N) { return ((size_t)N + 127) / 128 * 128; }
 
@@ -224,6 +243,11 @@ attn_status_t attn_fwd_layout(const void* q, const void* k, const void* v, void*
     a.fp16 = dtype == ATTN_FP16;
     a.num_sms = di.sms;
     a.error = di.err_ptr;
+    a.sched = nullptr;
+    if (a.seq.cu) {  // packed sequences: dynamic distribution
+        a.sched = take_sched_counter(di, static_cast<cudaStream_t>(stream));
+        if (!a.sched) return ATTN_ERR_CUDA;
+    }
     if (launch_fwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     t_last_launches = 1;
     return ATTN_OK;

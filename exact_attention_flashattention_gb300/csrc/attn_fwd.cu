@@ -37,6 +37,18 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units (b200-attention, Chapter 11)
 constexpr int kPanelBytes = 128 * 128;     // 128 rows x 128 bytes (64 16-bit elements)
 
+// Dynamic work distribution: one thread of the CTA takes units from a global counter (so a CTA
+// that finishes early takes more, which balances units of unequal work, e.g. packed sequences
+// of different lengths) and publishes them, in order, through a ring in shared memory; -1 ends
+// the sequence.  Every role reads the same sequence and expands each unit into its items.  Each
+// entry is held until its unit is done, and the scheduler claims entry k only once every
+// consumer has released entry k - 1 - kSchedAhead, so a CTA holds at most kSchedAhead units
+// beyond the one it works on: enough to hide the atomic's latency, little to hold back at the
+// end of the work.
+constexpr int kSchedDepth = 4;
+constexpr int kSchedAhead = 1;
+static_assert(kSchedAhead + 1 <= kSchedDepth, "a slot is rewritten only after its entry was released");
+
 template <int D>
 struct FwdLayout {
     static constexpr int kTile = 128 * D * 2;          // bytes of a 128-row tile
@@ -56,7 +68,10 @@ struct FwdLayout {
     static constexpr int kBarStats = kBarODone + 2;          // [2]
     static constexpr int kBarFin = kBarStats + 2;            // [2 stages][2 buffers]
     static constexpr int kBarTeardown = kBarFin + 4;
-    static constexpr int kNumBars = kBarTeardown + 1;
+    static constexpr int kBarSchedFull = kBarTeardown + 1;  // [kSchedDepth]
+    static constexpr int kBarSchedEmpty = kBarSchedFull + kSchedDepth;  // [kSchedDepth]
+    static constexpr int kNumBars = kBarSchedEmpty + kSchedDepth;
+    static constexpr int kSchedSlotWord = 2 * kNumBars;  // int index of the ring's 4 unit slots, after the barriers
     static constexpr int kScaleOff = kAux + 8 * 64;                // float [2][128]
     static constexpr int kFinLOff = kScaleOff + 2 * 128 * 4;       // float [2 buf][2 q][128]
     static constexpr int kFinMOff = kFinLOff + 4 * 128 * 4;        // float [2 buf][2 q][128]
@@ -64,7 +79,7 @@ struct FwdLayout {
     static constexpr int kBytes = kMiscOff + 64;
     static constexpr int kTmemS = 0;     // S_q at kTmemS + 128 q
     static constexpr int kTmemO = 256;   // O_q at kTmemO + 128 q
-    static_assert(kNumBars <= 64, "barrier area");
+    static_assert(2 * kNumBars + kSchedDepth <= 2 * 64, "barrier area (barriers and the unit ring)");
 };
 
 struct WorkItem {
@@ -108,13 +123,29 @@ __device__ __forceinline__ bool fwd_item(int u, int s, int M, int causal, const 
     return true;
 }
 
-// This CTA's sequence of work items: units blockIdx.x, blockIdx.x + gridDim.x, ...
-// (position kept as 2 * unit + slot in one register).
-struct FwdIter {
-    int pos;
-    __device__ FwdIter() : pos(2 * (int)blockIdx.x) {}
-    template <bool kTM>
-    __device__ bool next(WorkItem& w, int M, int causal, const SeqDesc& seq, int n_units) {
+// Consumer threads of the dynamic distribution: the three 128-thread warpgroups, the MMA warp
+// and the two loader threads.
+constexpr int kSchedConsumers = 3 * 128 + 32 + 2;
+
+// This CTA's sequence of work items.  kDyn = false: units blockIdx.x, blockIdx.x + gridDim.x, ...
+// (balanced when every unit holds the same work; the position is 2 unit + slot).  kDyn = true:
+// the units the scheduler thread publishes through the ring, which lives in the barrier area:
+// full[kSchedDepth] (one arrival, the scheduler thread), empty[kSchedDepth] (one arrival per
+// consumer thread) and the slot words themselves.  A consumer thread holds the entry of its
+// current unit until it takes the next one, so the unit index can be read again from shared
+// memory and the whole position is one register: 4 (entries taken) + (next item of the unit,
+// 2 = none left).  Every consumer thread releases entries itself (no warp-collective step, so a
+// thread that has stopped early cannot hold up its warp).  next() is false at the end of the
+// work, or when a wait gave up.
+template <bool kDyn>
+struct FwdIter;
+
+template <>
+struct FwdIter<false> {
+    int pos = 2 * (int)blockIdx.x;
+    template <bool kTM, class L>
+    __device__ bool next(WorkItem& w, int M, int causal, const SeqDesc& seq, int n_units, uint64_t*,
+                         const WaitGuard&, int) {
         for (;;) {
             const int u = pos >> 1, s = pos & 1;
             if (u >= n_units) return false;
@@ -124,11 +155,40 @@ struct FwdIter {
     }
 };
 
-template <int D, bool BF16, bool kTM>
+template <>
+struct FwdIter<true> {
+    uint32_t st = 2;
+    template <bool kTM, class L>
+    __device__ bool next(WorkItem& w, int M, int causal, const SeqDesc& seq, int, uint64_t* bars, const WaitGuard& g,
+                         int code) {
+        volatile int* ring = reinterpret_cast<volatile int*>(bars) + L::kSchedSlotWord;
+        for (;;) {
+            const uint32_t k = st >> 2, s = st & 3;
+            if (s < 2) {
+                ++st;
+                if (fwd_item<kTM>(ring[(k - 1) % kSchedDepth], (int)s, M, causal, seq, w)) return true;
+                continue;
+            }
+            if (k > 0) mbar_arrive(&bars[L::kBarSchedEmpty + (k - 1) % kSchedDepth]);
+            if (!mbar_wait(&bars[L::kBarSchedFull + k % kSchedDepth], (k / kSchedDepth) & 1, g, code)) return false;
+            if (ring[k % kSchedDepth] < 0) return false;
+            st = 4 * (k + 1);
+        }
+    }
+    // The item next() returned last, expanded again (lets a role keep only part of it live).
+    template <bool kTM, class L>
+    __device__ void current(WorkItem& w, int M, int causal, const SeqDesc& seq, uint64_t* bars) const {
+        const volatile int* ring = reinterpret_cast<volatile int*>(bars) + L::kSchedSlotWord;
+        fwd_item<kTM>(ring[((st >> 2) - 1) % kSchedDepth], (int)(st & 3) - 1, M, causal, seq, w);
+    }
+};
+
+template <int D, bool BF16, bool kTM, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, void* __restrict__ o_out,
-                float* __restrict__ lse_out, const SeqDesc seq, float scale, int causal, int* error) {
+                float* __restrict__ lse_out, const SeqDesc seq, float scale, int causal,
+                unsigned int* __restrict__ sched, int* error) {
     using L = FwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align the dynamic shared memory base to 1024 bytes (128B-swizzle atoms).
@@ -162,6 +222,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             mbar_init(&bars[L::kBarFin + 2 * q + 1], 128);
         }
         mbar_init(&bars[L::kBarTeardown], 1);
+        if (kDyn) {
+            for (int i = 0; i < kSchedDepth; ++i) {
+                mbar_init(&bars[L::kBarSchedFull + i], 1);
+                mbar_init(&bars[L::kBarSchedEmpty + i], kSchedConsumers);
+            }
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -193,7 +259,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         int k = 0;
         bool ok = true;
         WorkItem w;
-        for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
+        for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutSoftmax); ++k) {
             const int t = q ? w.t1 : w.t0;
             const int n = q ? w.n1 : w.n0;
             const int diag = (causal && t < w.T) ? t : -1;
@@ -280,22 +346,27 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         regs_dec<72>();
         const int row = threadIdx.x & 127;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-        uint32_t stats_phase[2] = {0, 0}, o_phase[2] = {0, 0};
-        int k = 0;
+        // Wait parities (bit q for Stats[q], bit 2 + q for ODone[q]) and, from bit 4 up, the
+        // number of items done: one register.
+        uint32_t ph = 0;
         bool ok = true;
-        WorkItem w;
-        for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
-            for (int j = 0; j < w.n1 && ok; ++j) {
+        FwdIter<kDyn> itr;
+        for (WorkItem w0; ok && itr.template next<kTM, L>(w0, M, causal, seq, n_units, bars, guard, kDevTimeoutCorr);
+             ph += 16) {
+            // With the dynamic distribution only the tile counts stay live through the loop and the
+            // epilogue expands the item again (the warpgroup has 72 registers).
+            const int n0 = w0.n0, n1 = w0.n1;
+            for (int j = 0; j < n1 && ok; ++j) {
 #pragma unroll
                 for (int q = 0; q < 2; ++q) {
-                    const int n = q ? w.n1 : w.n0;
+                    const int n = q ? n1 : n0;
                     if (j >= n) continue;
-                    if (!mbar_wait(&bars[L::kBarStats + q], stats_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
-                    stats_phase[q] ^= 1;
+                    if (!mbar_wait(&bars[L::kBarStats + q], (ph >> q) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                    ph ^= 1u << q;
                     const float alpha = scale_buf[q * 128 + row];
                     if (j > 0) {
-                        if (!mbar_wait(&bars[L::kBarODone + q], o_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
-                        o_phase[q] ^= 1;
+                        if (!mbar_wait(&bars[L::kBarODone + q], (ph >> (2 + q)) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                        ph ^= 4u << q;
                         tc_fence_after();
                         if (__any_sync(0xffffffffu, alpha != 1.f)) {
                             const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
@@ -317,11 +388,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             if (!ok) break;
             // epilogue: O = O / l -> 16-bit, L = (m + log2 l) ln 2
+            WorkItem w;
+            if constexpr (kDyn) itr.template current<kTM, L>(w, M, causal, seq, bars);
+            else w = w0;
             for (int q = 0; q < 2 && ok; ++q) {
-                const int b = k & 1;
-                if (!mbar_wait(&bars[L::kBarODone + q], o_phase[q], guard, kDevTimeoutCorr)) { ok = false; break; }
-                o_phase[q] ^= 1;
-                if (!mbar_wait(&bars[L::kBarFin + 2 * q + b], (k >> 1) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                const uint32_t b = (ph >> 4) & 1;
+                if (!mbar_wait(&bars[L::kBarODone + q], (ph >> (2 + q)) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
+                ph ^= 4u << q;
+                if (!mbar_wait(&bars[L::kBarFin + 2 * q + b], (ph >> 5) & 1, guard, kDevTimeoutCorr)) { ok = false; break; }
                 tc_fence_after();
                 const float l = fin_l[(b * 2 + q) * 128 + row];
                 const float mrow = fin_m[(b * 2 + q) * 128 + row];
@@ -330,19 +404,23 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 const float inv_l = 1.f / l;
                 const uint32_t o_addr = tmem + lane_base + L::kTmemO + 128 * q;
                 uint8_t* dst = reinterpret_cast<uint8_t*>(o_out) + seq_row_offset<kTM>(seq, w.si, grow, D) * 2;
+                // Token-major rows need more address registers: 16 columns per TMEM load keeps the
+                // warpgroup inside its 72 registers.
+                constexpr int kCols = kTM ? 16 : 32;
 #pragma unroll 1
-                for (int c = 0; c < D; c += 32) {
-                    uint32_t r[32];
-                    tmem_ld32(o_addr + c, r);
+                for (int c = 0; c < D; c += kCols) {
+                    uint32_t r[kCols];
+                    if constexpr (kCols == 32) tmem_ld32(o_addr + c, r);
+                    else tmem_ld16(o_addr + c, r);
                     tmem_wait_ld();
-                    uint32_t pk[16];
+                    uint32_t pk[kCols / 2];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e)
+                    for (int e = 0; e < kCols / 2; ++e)
                         pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]) * inv_l, __uint_as_float(r[2 * e + 1]) * inv_l);
                     if (grow < w.si.len) {
                         uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
-                        for (int e = 0; e < 4; ++e)
+                        for (int e = 0; e < kCols / 8; ++e)
                             d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                     }
                 }
@@ -387,7 +465,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 return r;
             };
             WorkItem w;
-            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units);) {
+            for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutMma);) {
                 if (!warp_mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
                 q_phase ^= 1;
                 tc_fence_after();
@@ -440,7 +518,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             bool ok = true;
             int last_q_item = -1;
             WorkItem w;
-            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units); ++k) {
+            for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad); ++k) {
                 if (k > 0 && !mbar_wait(&bars[L::kBarQEmpty], (k - 1) & 1, guard, kDevTimeoutLoad)) { ok = false; break; }
                 mbar_arrive_expect_tx(&bars[L::kBarQFull], 2 * L::kTile);
                 last_q_item = k;
@@ -457,7 +535,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t tok = 0;
             bool ok = true;
             WorkItem w;
-            for (FwdIter itr; ok && itr.template next<kTM>(w, M, causal, seq, n_units);) {
+            for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad);) {
                 for (int j = 0; j < w.n1 && ok; ++j) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
@@ -480,6 +558,21 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // Let every copy issued above land before shared memory is released.
             for (uint32_t t = (tok > (uint32_t)L::kStages ? tok - L::kStages : 0); t < tok; ++t)
                 mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
+        } else if (kDyn && warp == 15 && lane == 0) {
+            // ------------------------------------------------------------ scheduler
+            // It waits with a sleep between polls: its warp shares a scheduler with softmax warps.
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t pos = k % kSchedDepth, e = k - 1 - kSchedAhead;  // e: entry to be released
+                if (k > (uint32_t)kSchedAhead &&
+                    !mbar_wait_sleep(&bars[L::kBarSchedEmpty + e % kSchedDepth], (e / kSchedDepth) & 1, guard,
+                                     kDevTimeoutLoad))
+                    break;
+                const unsigned int u = atomicAdd(sched, 1u);
+                const int val = u < (unsigned int)n_units ? (int)u : -1;
+                reinterpret_cast<volatile int*>(bars)[L::kSchedSlotWord + pos] = val;
+                mbar_arrive(&bars[L::kBarSchedFull + pos]);  // release: the slot is written first
+                if (val < 0) break;
+            }
         }
     }
 
@@ -491,11 +584,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     }
 }
 
-template <int D, bool BF16, bool kTM>
+template <int D, bool BF16, bool kTM, bool kDyn>
 cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     using L = FwdLayout<D>;
     const int smem_bytes = L::kBytes + 1024;  // + alignment slack
-    auto kern = attn_fwd_kernel<D, BF16, kTM>;
+    auto kern = attn_fwd_kernel<D, BF16, kTM, kDyn>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     const int T = (a.N + 127) / 128;
@@ -504,21 +597,27 @@ cudaError_t launch_fwd_t(const FwdArgs& a, cudaStream_t stream) {
     const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
     if (grid <= 0) return cudaSuccess;
     kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.o, a.lse, a.seq, a.scale, a.causal,
-                                                  a.error);
+                                                  a.sched, a.error);
     return cudaGetLastError();
 }
 
-template <bool kTM>
+template <bool kTM, bool kDyn>
 cudaError_t launch_fwd_l(const FwdArgs& a, cudaStream_t stream) {
-    if (a.d == 128) return a.fp16 ? launch_fwd_t<128, false, kTM>(a, stream) : launch_fwd_t<128, true, kTM>(a, stream);
-    if (a.d == 64) return a.fp16 ? launch_fwd_t<64, false, kTM>(a, stream) : launch_fwd_t<64, true, kTM>(a, stream);
+    if (a.d == 128)
+        return a.fp16 ? launch_fwd_t<128, false, kTM, kDyn>(a, stream) : launch_fwd_t<128, true, kTM, kDyn>(a, stream);
+    if (a.d == 64)
+        return a.fp16 ? launch_fwd_t<64, false, kTM, kDyn>(a, stream) : launch_fwd_t<64, true, kTM, kDyn>(a, stream);
     return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
+// Row layout and work distribution: [B, H, N, d] and BSHD hold sequences of one length, whose
+// units all carry the same work, so the static distribution is balanced and costs nothing;
+// packed sequences of different lengths take units from the launch's work counter.
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream) {
-    return a.seq.token_major ? launch_fwd_l<true>(a, stream) : launch_fwd_l<false>(a, stream);
+    if (!a.seq.token_major) return launch_fwd_l<false, false>(a, stream);
+    return a.seq.cu ? launch_fwd_l<true, true>(a, stream) : launch_fwd_l<true, false>(a, stream);
 }
 
 }  // namespace gb300

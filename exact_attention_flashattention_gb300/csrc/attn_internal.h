@@ -43,6 +43,7 @@ struct FwdArgs {
     int causal;
     int fp16;         // 0 = bf16, 1 = fp16
     int num_sms;
+    unsigned int* sched;  // packed sequences: work counter of this launch, zero at launch
     int* error;       // device error word
 };
 

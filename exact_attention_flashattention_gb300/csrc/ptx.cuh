@@ -74,6 +74,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Bounded wait with a short sleep between polls, for a thread whose warp should leave issue
+// slots to busier warps on the same scheduler.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, const WaitGuard& g, int code) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*g.abort) return false;
+        if (globaltimer_ns() - t0 > g.limit_ns) {
+            *g.abort = 1;
+            atomicCAS(g.error, 0, code);
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
+
 // The same wait taken by all 32 lanes of a warp, with a warp-uniform outcome
 // (a lane that gives up makes the whole warp give up).
 __device__ __forceinline__ bool warp_mbar_wait(uint64_t* bar, uint32_t parity, const WaitGuard& g, int code) {

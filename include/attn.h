@@ -101,7 +101,10 @@ ATTN_API attn_status_t attn_fwd_ex(const void *q, const void *k, const void *v, 
  * other layouts).  Offsets that break these rules are detected on the device:
  * the offending sequences are skipped (their outputs are not written) and
  * attn_last_device_error() returns ATTN_ERR_INVALID_ARG.  With
- * total_tokens == 0 nothing is queued.
+ * total_tokens == 0 nothing is queued.  For ATTN_LAYOUT_PACKED the call also
+ * queues, before the kernel, a 4-byte memset of one of the library's 1024
+ * per-launch work counters (taken round robin), so at most 1024 packed
+ * forwards may be in flight at once across all streams of a device.
  */
 ATTN_API attn_status_t attn_fwd_layout(const void *q, const void *k, const void *v, void *o, float *lse,
                               int B, int H, int max_seqlen, int d, float scale, int causal,
