@@ -14,6 +14,10 @@ O = PV; backward: dV = P^T dO, dP = dO V^T, D = rowsum(dO o O),
 dS = P o (dP - D), dQ = dS K/sqrt(d), dK = dS^T Q/sqrt(d)), with the caller's
 ``scale`` in place of 1/sqrt(d).
 
+The sparse top-k attention with a shared latent key/value row (``dsa.py``,
+numpy in double precision) is re-exported here as ``dsa_fwd`` / ``dsa_bwd``;
+its pins are in ``tests/test_oracle_dsa.py``.
+
 Parity pins: every function here is pinned by ``tests/test_oracle.py``
 (finite differences of a scalar loss, the Q = 0 closed form, row-sum
 invariants of P and dS, N = 1 and first-row special cases, shift and
@@ -200,6 +204,9 @@ def attn_probs(q, k, v, scale: float, causal: bool, dout=None):
     if rc != 0:
         raise RuntimeError(f"oracle_attn_probs failed ({rc})")
     return P, dS
+
+
+from .dsa import dsa_bwd, dsa_fwd  # noqa: E402  (numpy; no C build needed)
 
 
 if __name__ == "__main__":  # pragma: no cover

@@ -28,7 +28,7 @@ GAMMA = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "do": 4}
+TENSOR_IDS = {"q": 1, "k": 2, "v": 3, "do": 4, "kv": 5, "sink": 6, "idx": 7}
 
 
 def _mix(z: np.ndarray) -> np.ndarray:
@@ -149,3 +149,50 @@ def late_spike(q_bits: np.ndarray, k_bits: np.ndarray, dtype: str, alpha: float,
         nrm = np.linalg.norm(q[i]) or 1.0
         k[j] = (alpha * q[i] / nrm).astype(np.float32)
     return to_bits(k, dtype)
+
+
+def _rows_normal(base_seed: int, name: str, rows, width: int, sigma: float) -> np.ndarray:
+    """float32 [len(rows), width]: row r drawn from its own stream (so one row can be
+    regenerated alone), entries ~ N(0, sigma^2)."""
+    tid = TENSOR_IDS[name]
+    out = np.empty((len(rows), width), dtype=np.float32)
+    for ix, r in enumerate(rows):
+        out[ix] = standard_normal(head_key(base_seed, tid, int(r)), width) * np.float32(sigma)
+    return out
+
+
+def topk_indices(base_seed: int, s_q: int, s_kv: int, topk: int, causal: bool, rows=None):
+    """Key index lists of a sparse top-k attention: for query i, min(topk, n_i) distinct
+    keys in random order, n_i = i + 1 when causal (keys 0..i) else s_kv, padded with -1.
+    Returns (idx int32 [len(rows), topk], lengths int32 [len(rows)]).  Each row is a
+    random permutation (keys sorted by a SplitMix64 draw), so rows are independent."""
+    rows = range(s_q) if rows is None else rows
+    rows = list(rows)
+    tid = TENSOR_IDS["idx"]
+    idx = np.full((len(rows), topk), -1, dtype=np.int32)
+    lens = np.empty(len(rows), dtype=np.int32)
+    for ix, i in enumerate(rows):
+        n = min(int(i) + 1, s_kv) if causal else s_kv
+        keys = splitmix64_stream(head_key(base_seed, tid, int(i)), n)
+        take = np.argsort(keys, kind="stable")[:min(topk, n)]
+        idx[ix, :take.shape[0]] = take.astype(np.int32)
+        lens[ix] = take.shape[0]
+    return idx, lens
+
+
+def dsa_inputs(base_seed: int, s_q: int, s_kv: int, H: int, d_qk: int, d_v: int, topk: int,
+               causal: bool, sigma: float = 1.0, rows=None, with_kv: bool = True) -> dict:
+    """Synthetic inputs of a sparse top-k attention with one shared latent key/value row
+    per key (bf16 bit patterns unless noted):
+      q [n, H, d_qk], do [n, H, d_v] for the query rows `rows` (default all s_q),
+      kv [s_kv, d_qk] (if with_kv), sink float32 [H], idx int32 [n, topk], lens int32 [n].
+    Values ~ N(0, sigma^2) for q, kv, do; sink ~ N(0, 1)."""
+    rows = list(range(s_q) if rows is None else rows)
+    out = {}
+    out["q"] = round_bf16_bits(_rows_normal(base_seed, "q", rows, H * d_qk, sigma)).reshape(len(rows), H, d_qk)
+    out["do"] = round_bf16_bits(_rows_normal(base_seed, "do", rows, H * d_v, sigma)).reshape(len(rows), H, d_v)
+    if with_kv:
+        out["kv"] = round_bf16_bits(_rows_normal(base_seed, "kv", range(s_kv), d_qk, sigma))
+    out["sink"] = standard_normal(head_key(base_seed, TENSOR_IDS["sink"], 0), H)
+    out["idx"], out["lens"] = topk_indices(base_seed, s_q, s_kv, topk, causal, rows)
+    return out
