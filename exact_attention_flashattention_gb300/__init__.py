@@ -13,6 +13,9 @@ Names mirror the C ABI:
     attn_bwd_layout_workspace_size(B, H, max_seqlen, d, layout, total_tokens)
     attn_decode(q, k_cache, v_cache, o, lse, workspace, scale, cache_seqlens=None, stream=None)
     attn_decode_workspace_size(B, Hq, Hkv, Nmax, d)
+    attn_dsa_bwd(q, kv, o, dout, lse, sink, topk_idx, topk_len, dq, dkv, dsink, workspace, scale, causal,
+                 stream=None)
+    attn_dsa_bwd_workspace_size(s_kv, d_qk)
     attn_last_device_error(stream=None)
 plus two allocating conveniences, ``forward`` and ``backward``.
 Tensors are contiguous CUDA tensors of bfloat16 or float16: [B, H, N, d] (layout
@@ -29,7 +32,8 @@ import threading
 __all__ = [
     "AttnError", "attn_fwd", "attn_bwd", "attn_bwd_stage", "attn_bwd_workspace_size", "attn_last_device_error",
     "attn_status_string", "attn_last_launch_count", "attn_fwd_layout", "attn_bwd_layout",
-    "attn_bwd_layout_workspace_size", "attn_decode", "attn_decode_workspace_size", "LAYOUTS", "forward",
+    "attn_bwd_layout_workspace_size", "attn_decode", "attn_decode_workspace_size", "attn_dsa_bwd",
+    "attn_dsa_bwd_workspace_size", "LAYOUTS", "forward",
     "backward", "decode", "library_path", "load",
 ]
 
@@ -46,7 +50,7 @@ EXPORTS = (
     "attn_fwd", "attn_fwd_ex", "attn_bwd_workspace_size", "attn_bwd", "attn_bwd_ex", "attn_bwd_stage",
     "attn_status_string", "attn_last_device_error", "attn_last_launch_count", "attn_fwd_layout",
     "attn_bwd_layout", "attn_bwd_layout_workspace_size", "attn_bwd_noalloc", "attn_decode",
-    "attn_decode_workspace_size",
+    "attn_decode_workspace_size", "attn_dsa_bwd", "attn_dsa_bwd_workspace_size",
 )
 
 
@@ -86,12 +90,15 @@ def load():
         lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, sz, i, i, i, i, i, f, i, vp]
         lib.attn_decode_workspace_size.argtypes = [i, i, i, i, i]
         lib.attn_decode_workspace_size.restype = sz
+        lib.attn_dsa_bwd.argtypes = [vp] * 11 + [vp, sz, i, i, i, i, i, i, f, i, vp]
+        lib.attn_dsa_bwd_workspace_size.argtypes = [i, i]
+        lib.attn_dsa_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i]
         lib.attn_status_string.restype = ctypes.c_char_p
         lib.attn_last_device_error.argtypes = [vp]
         lib.attn_last_launch_count.argtypes = []
         for fn in (lib.attn_fwd, lib.attn_fwd_ex, lib.attn_bwd, lib.attn_bwd_ex, lib.attn_bwd_stage,
-                   lib.attn_fwd_layout, lib.attn_bwd_layout, lib.attn_decode,
+                   lib.attn_fwd_layout, lib.attn_bwd_layout, lib.attn_decode, lib.attn_dsa_bwd,
                    lib.attn_last_device_error,
                    lib.attn_last_launch_count):
             fn.restype = ctypes.c_int
@@ -239,6 +246,35 @@ def attn_decode(q, k_cache, v_cache, o, lse, workspace, scale: float, cache_seql
                          _dtype_code(q), _stream_handle(stream))
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode")
+
+
+def attn_dsa_bwd_workspace_size(s_kv: int, d_qk: int) -> int:
+    return int(load().attn_dsa_bwd_workspace_size(int(s_kv), int(d_qk)))
+
+
+def attn_dsa_bwd(q, kv, o, dout, lse, sink, topk_idx, topk_len, dq, dkv, dsink, workspace, scale: float,
+                 causal: bool, stream=None) -> None:
+    """Queue the sparse top-k attention backward (shared latent key/value rows).
+    q, dq: bf16 [s_q, H, d_qk]; kv, dkv: bf16 [s_kv, d_qk]; o, dout: bf16 [s_q, H, 512];
+    lse: float32 [s_q, H]; sink, dsink: float32 [H] or None; topk_idx: int32 [s_q, topk];
+    topk_len: int32 [s_q] or None; workspace: at least attn_dsa_bwd_workspace_size bytes."""
+    import torch
+    lib = load()
+    s_q, H, d_qk = q.shape
+    s_kv = kv.shape[0]
+    d_v = o.shape[2]
+    topk = topk_idx.shape[1]
+    for t, n in ((topk_idx, "topk_idx"), (topk_len, "topk_len")):
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError(f"{n} must be int32")
+    opt = lambda t, n: None if t is None else _check(t, n)
+    st = lib.attn_dsa_bwd(_check(q, "q"), _check(kv, "kv"), _check(o, "o"), _check(dout, "dout"), _check(lse, "lse"),
+                          opt(sink, "sink"), _check(topk_idx, "topk_idx"), opt(topk_len, "topk_len"), _check(dq, "dq"),
+                          _check(dkv, "dkv"), opt(dsink, "dsink"), _check(workspace, "workspace"),
+                          workspace.numel() * workspace.element_size(), s_q, s_kv, H, d_qk, d_v, topk, float(scale),
+                          int(bool(causal)), _stream_handle(stream))
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_dsa_bwd")
 
 
 def attn_last_device_error(stream=None) -> int:

@@ -106,6 +106,20 @@ bool make_map_seq(CUtensorMap* m, const void* base, const SeqDesc& s, int d) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// [rows, width] 16-bit row array viewed as {width, rows, 1}, box {64, box_rows, 1}.
+bool make_map_rows(CUtensorMap* m, const void* base, int rows, int width, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)width * 2, (cuuint64_t)rows * width * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // A zeroed work counter for one launch on `stream` (nullptr if the memset could not be queued).
 unsigned int* take_sched_counter(const DevInfo& di, cudaStream_t stream) {
     static std::atomic<unsigned int> next{0};
@@ -418,6 +432,63 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     a.num_sms = di.sms;
     a.error = di.err_ptr;
     if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+    t_last_launches = 2;
+    return ATTN_OK;
+}
+
+size_t attn_dsa_bwd_workspace_size(int s_kv, int d_qk) {
+    if (s_kv <= 0 || (d_qk != 512 && d_qk != 576)) return 0;
+    return align_up((size_t)s_kv * d_qk * sizeof(float), 256);
+}
+
+attn_status_t attn_dsa_bwd(const void* q, const void* kv, const void* o, const void* dout, const float* lse,
+                           const float* sink, const int* topk_idx, const int* topk_len, void* dq, void* dkv,
+                           float* dsink, void* workspace, size_t workspace_bytes, int s_q, int s_kv, int H, int d_qk,
+                           int d_v, int topk, float scale, int causal, void* stream) {
+    t_last_launches = 0;
+    if (!q || !kv || !o || !dout || !lse || !topk_idx || !dq || !dkv) return ATTN_ERR_INVALID_ARG;
+    if (sink && !dsink) return ATTN_ERR_INVALID_ARG;
+    if (s_q <= 0 || s_kv <= 0 || H <= 0 || topk <= 0) return ATTN_ERR_INVALID_ARG;
+    if (H % 64 != 0 || (d_qk != 512 && d_qk != 576) || d_v != 512) return ATTN_ERR_UNSUPPORTED;
+    if ((long long)s_q * H * d_qk >= (1ll << 31) || (long long)s_kv * d_qk >= (1ll << 31) ||
+        (long long)s_q * topk >= (1ll << 31))
+        return ATTN_ERR_UNSUPPORTED;
+    const size_t need = attn_dsa_bwd_workspace_size(s_kv, d_qk);
+    if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return ATTN_ERR_ALIGNMENT;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) || !aligned16(dkv))
+        return ATTN_ERR_ALIGNMENT;
+    auto a4 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; };
+    if (!a4(lse) || !a4(topk_idx) || (sink && !a4(sink)) || (sink && !a4(dsink)) || (topk_len && !a4(topk_len)))
+        return ATTN_ERR_ALIGNMENT;
+    DevInfo di;
+    if (!dev_info(di)) return ATTN_ERR_CUDA;
+    DsaArgs a;
+    std::memset(&a, 0, sizeof(a));
+    // q and dO as 2-D row arrays [s_q H, width]; one box = 64 heads x 64 columns.
+    if (!make_map_rows(&a.tm_q, q, s_q * H, d_qk, 64) || !make_map_rows(&a.tm_do, dout, s_q * H, d_v, 64))
+        return ATTN_ERR_CUDA;
+    a.kv = kv;
+    a.o = o;
+    a.dout = dout;
+    a.lse = lse;
+    a.sink = sink;
+    a.idx = topk_idx;
+    a.topk_len = topk_len;
+    a.dq = dq;
+    a.dkv = dkv;
+    a.dkv_acc = static_cast<float*>(workspace);
+    a.dsink = sink ? dsink : nullptr;
+    a.s_q = s_q;
+    a.s_kv = s_kv;
+    a.H = H;
+    a.d_qk = d_qk;
+    a.topk = topk;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.num_sms = di.sms;
+    a.error = di.err_ptr;
+    if (launch_dsa_bwd(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
     t_last_launches = 2;
     return ATTN_OK;
 }

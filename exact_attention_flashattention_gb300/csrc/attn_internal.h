@@ -89,7 +89,31 @@ struct DecodeArgs {
     int* error;
 };
 
+// Sparse top-k attention backward with a shared latent key/value row (dsa_bwd.cu).
+struct DsaArgs {
+    CUtensorMap tm_q;        // q  [s_q H, d_qk] 16-bit, box 64 columns x 64 rows, 128B swizzle
+    CUtensorMap tm_do;       // dO [s_q H, 512], same box
+    const void* kv;          // [s_kv, d_qk] bf16
+    const void* o;           // [s_q, H, 512] bf16
+    const void* dout;        // [s_q, H, 512] bf16
+    const float* lse;        // [s_q, H]
+    const float* sink;       // [H] or nullptr
+    const int* idx;          // [s_q, topk]
+    const int* topk_len;     // [s_q] or nullptr
+    void* dq;                // [s_q, H, d_qk] bf16
+    void* dkv;               // [s_kv, d_qk] bf16
+    float* dkv_acc;          // [s_kv, d_qk] FP32 workspace
+    float* dsink;            // [H] or nullptr
+    int s_q, s_kv, H, d_qk, topk;
+    float scale;
+    int causal;
+    int num_sms;
+    int* error;
+};
+
 cudaError_t launch_fwd(const FwdArgs& a, cudaStream_t stream);
+// Zeroes the accumulators, then the main kernel and the dKV conversion (two kernels).
+cudaError_t launch_dsa_bwd(const DsaArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // stage: -1 = all three kernels; 0 = preprocess; 1 = main kernel; 2 = dQ conversion.
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage);

@@ -236,6 +236,46 @@ ATTN_API attn_status_t attn_decode(const void *q, const void *k_cache, const voi
                           size_t workspace_bytes, int B, int Hq, int Hkv, int Nmax, int d,
                           float scale, attn_dtype_t dtype, void *stream);
 
+/*
+ * Backward of sparse top-k attention with one shared latent key/value row per
+ * key, the workload of "Improve performance of SM100 DSA backward kernel"
+ * (cudnn-frontend pull request 684, PR description): every head of query row i
+ * attends to the keys its top-k list names, gathered from one latent row per
+ * key; K is the whole row (d_qk = 512 or 576 columns) and V its first d_v = 512
+ * columns; an optional per-head sink logit joins each softmax with no value
+ * row.  With e the valid entries of row i's list (position e < len_i, where
+ * len_i = min(topk_len[i], topk) or topk if topk_len is NULL;
+ * 0 <= topk_idx[i, e] < s_kv; and topk_idx[i, e] <= i when causal), and the
+ * forward's O and L (L including the sink), the call computes, as in the dense
+ * backward ("Writing Speed-of-Light Attention Backward Kernel for 5090 in
+ * CUDA", "Mathematical Formulation"):
+ *   D = dO . O,  P_e = exp(scale q . k_e - L),  dS_e = P_e (dO . v_e - D)
+ *   dq   = scale sum_e dS_e k_e
+ *   dkv[topk_idx[i, e]] += scale dS_e q (all d_qk columns) + P_e dO (first 512)
+ *   dsink_h = - sum_i exp(sink_h - L_ih) D_ih
+ * A key listed twice in a row counts twice.  Rows with no valid entry get dq = 0.
+ *
+ * Layouts (all DEVICE pointers, caller-owned, bf16 unless noted):
+ *   q [s_q, H, d_qk], kv [s_kv, d_qk], o and dout [s_q, H, 512],
+ *   lse FP32 [s_q, H] (natural log), sink FP32 [H] or NULL,
+ *   topk_idx int32 [s_q, topk], topk_len int32 [s_q] or NULL;
+ *   outputs dq [s_q, H, d_qk], dkv [s_kv, d_qk] (overwritten), dsink FP32 [H]
+ *   (overwritten; required when sink is given, ignored otherwise).
+ * Requires H a multiple of 64, d_qk 512 or 576, d_v 512, topk >= 1,
+ * s_q, s_kv >= 1, s_q H d_qk and s_kv d_qk below 2^31, 16-byte aligned
+ * tensors (4-byte for lse, sink, dsink, topk_idx, topk_len), and a workspace
+ * of attn_dsa_bwd_workspace_size() bytes, 256-byte aligned (the FP32 dkv
+ * accumulator).  Queues two kernels (after two memsets).  Returns a status
+ * before any launch on bad arguments.
+ */
+ATTN_API size_t attn_dsa_bwd_workspace_size(int s_kv, int d_qk);
+ATTN_API attn_status_t attn_dsa_bwd(const void *q, const void *kv, const void *o, const void *dout,
+                                    const float *lse, const float *sink, const int *topk_idx,
+                                    const int *topk_len, void *dq, void *dkv, float *dsink,
+                                    void *workspace, size_t workspace_bytes, int s_q, int s_kv,
+                                    int H, int d_qk, int d_v, int topk, float scale, int causal,
+                                    void *stream);
+
 /* Static string naming a status code. */
 ATTN_API const char *attn_status_string(attn_status_t status);
 

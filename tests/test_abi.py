@@ -132,3 +132,39 @@ def test_decode_argument_checks_before_any_launch(lib):
     assert d(p, p, p, p, p, vp(258), p, n, 2, 8, 2, 1000, 128, 1.0, 0, null) == 3          # lengths alignment
     assert d(p, p, p, p, p, null, p, n, 2, 8, 2, 1000, 128, 1.0, 5, null) == 1             # bad dtype
     assert lib.attn_last_launch_count() == 0
+
+
+def test_dsa_argument_checks_before_any_launch(lib):
+    import exact_attention_flashattention_gb300 as attn
+    vp = ctypes.c_void_p
+    p = vp(256)
+    null = vp(0)
+    f = lib.attn_dsa_bwd
+    wsz = attn.attn_dsa_bwd_workspace_size
+    assert wsz(1000, 576) == (1000 * 576 * 4 + 255) // 256 * 256
+    assert wsz(1000, 128) == 0                # d_qk unsupported
+    n = wsz(100, 576)
+    # q kv o dout lse sink idx len dq dkv dsink ws bytes s_q s_kv H d_qk d_v topk scale causal stream
+    ok = [p, p, p, p, p, null, p, null, p, p, null, p, n, 10, 100, 64, 576, 512, 64, 0.1, 0, null]
+
+    def call(**kw):
+        a = list(ok)
+        names = ["q", "kv", "o", "dout", "lse", "sink", "idx", "len", "dq", "dkv", "dsink", "ws", "bytes",
+                 "s_q", "s_kv", "H", "d_qk", "d_v", "topk", "scale", "causal", "stream"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return f(*a)
+
+    assert call(q=null) == 1                  # null pointer
+    assert call(sink=p) == 1                  # sink without dsink
+    assert call(s_q=0) == 1
+    assert call(topk=0) == 1
+    assert call(H=96) == 2                    # H not a multiple of 64
+    assert call(d_qk=256) == 2
+    assert call(d_v=256) == 2
+    assert call(ws=null) == 4
+    assert call(bytes=n - 1) == 4
+    assert call(ws=vp(256 + 16)) == 3         # workspace alignment
+    assert call(q=vp(258)) == 3               # tensor alignment
+    assert call(idx=vp(258)) == 3
+    assert lib.attn_last_launch_count() == 0

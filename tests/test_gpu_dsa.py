@@ -1,0 +1,130 @@
+"""Sparse top-k attention backward (shared latent key/value rows) vs the FP64 oracle,
+through the C ABI.
+
+Inputs: q, kv, dO from the seeded generator (bf16), top-k lists of distinct random
+keys (causal rows draw from keys 0..i and are padded with -1), a sink per head.  O and
+L are the oracle forward's, rounded as the kernel receives them (O to bf16, L to
+FP32), and the oracle backward is given the same rounded values, so both sides
+compute the backward of the same inputs.  Some cases add padding entries, indices
+outside [0, s_kv), duplicates, keys after the query (masked when causal), shortened
+rows and an empty row.  Bounds: dQ and dKV relative Frobenius error <= 1e-2 (the
+gradient tolerance of the dense path), dSink <= 1e-3.  Outputs are pre-filled with
+NaN so an unwritten element fails.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from attn_cases import TOL_GRAD_RELFRO, rel_fro
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # s_q, s_kv, H, d_qk, topk, causal, sink, perturb
+    (40, 300, 64, 576, 256, False, True, False),
+    (48, 200, 128, 512, 192, True, True, False),
+    (32, 500, 64, 576, 384, False, True, True),
+    (24, 64, 64, 512, 128, True, False, True),
+    (16, 1000, 128, 576, 100, False, True, True),
+]
+TOL_DSINK = 1e-3
+
+
+@pytest.fixture(scope="module")
+def attn():
+    import exact_attention_flashattention_gb300 as a
+    a.load()
+    return a
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+
+def _f64(bits):
+    return si.bf16_bits_to_f32(bits).astype(np.float64)
+
+
+def _perturb(idx, lens, s_q, s_kv, seed):
+    """Padding, out-of-range indices, duplicates, keys after the query, a shortened
+    row and an empty row."""
+    rng = np.random.default_rng(seed)
+    idx = idx.copy()
+    lens = lens.copy()
+    topk = idx.shape[1]
+    for i in range(s_q):
+        e = rng.integers(0, topk, size=4)
+        idx[i, e[0]] = -1
+        idx[i, e[1]] = s_kv + int(rng.integers(0, 7))
+        idx[i, e[2]] = idx[i, e[3]]                        # duplicate (may be -1)
+        idx[i, int(rng.integers(0, topk))] = int(rng.integers(0, s_kv))   # possibly after the query
+    lens[1] = topk // 3
+    lens[2] = 0
+    lens[3] = topk + 5                                       # clamped to topk
+    return idx, lens
+
+
+def _run_case(attn, s_q, s_kv, H, d_qk, topk, causal, sink, perturb, seed):
+    d_v, scale = 512, 1.0 / math.sqrt(d_qk)
+    x = si.dsa_inputs(seed, s_q, s_kv, H, d_qk, d_v, topk, causal)
+    idx, lens = x["idx"], x["lens"]
+    if perturb:
+        idx, lens = _perturb(idx, lens, s_q, s_kv, seed)
+    use_len = perturb or causal
+    snk = x["sink"].astype(np.float64) if sink else None
+    q, kv, do = _f64(x["q"]), _f64(x["kv"]), _f64(x["do"])
+    o_ref, l_ref = oracle.dsa_fwd(q, kv, snk, idx, lens if use_len else None, scale, causal, d_v)
+    o_bits = si.round_bf16_bits(o_ref.astype(np.float32))
+    l32 = l_ref.astype(np.float32)
+    ref = oracle.dsa_bwd(q, kv, _f64(o_bits), do, l32.astype(np.float64), snk, idx,
+                         lens if use_len else None, scale, causal, d_v)
+
+    dev = dict(q=_bf16_dev(x["q"]), kv=_bf16_dev(x["kv"]), do=_bf16_dev(x["do"]), o=_bf16_dev(o_bits))
+    lse = torch.from_numpy(l32).to("cuda")
+    sink_t = torch.from_numpy(x["sink"]).to("cuda") if sink else None
+    idx_t = torch.from_numpy(np.ascontiguousarray(idx)).to("cuda")
+    len_t = torch.from_numpy(np.ascontiguousarray(lens)).to("cuda") if use_len else None
+    dq = torch.full((s_q, H, d_qk), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dkv = torch.full((s_kv, d_qk), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dsink = torch.full((H,), float("nan"), dtype=torch.float32, device="cuda") if sink else None
+    ws = torch.empty(attn.attn_dsa_bwd_workspace_size(s_kv, d_qk), dtype=torch.uint8, device="cuda")
+    attn.attn_dsa_bwd(dev["q"], dev["kv"], dev["o"], dev["do"], lse, sink_t, idx_t, len_t, dq, dkv, dsink, ws,
+                      scale, causal)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+    got_dq = dq.float().cpu().numpy().astype(np.float64)
+    got_dkv = dkv.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got_dq).all() and np.isfinite(got_dkv).all()
+    e_dq, e_dkv = rel_fro(got_dq, ref["dq"]), rel_fro(got_dkv, ref["dkv"])
+    assert e_dq <= TOL_GRAD_RELFRO, ("dq", e_dq)
+    assert e_dkv <= TOL_GRAD_RELFRO, ("dkv", e_dkv)
+    if perturb:
+        assert np.all(got_dq[2] == 0.0)                      # the empty row
+    if sink:
+        got_ds = dsink.cpu().numpy().astype(np.float64)
+        e_ds = rel_fro(got_ds, ref["dsink"])
+        assert e_ds <= TOL_DSINK, ("dsink", e_ds)
+    return e_dq, e_dkv
+
+
+@pytest.mark.parametrize("s_q,s_kv,H,d_qk,topk,causal,sink,perturb", CASES)
+def test_dsa_bwd_matches_oracle(attn, s_q, s_kv, H, d_qk, topk, causal, sink, perturb):
+    _run_case(attn, s_q, s_kv, H, d_qk, topk, causal, sink, perturb, seed=700 + s_q + topk)
+
+
+def test_dsa_bwd_argument_errors(attn):
+    """Unsupported shapes are refused before any launch."""
+    q = torch.zeros((4, 32, 576), dtype=torch.bfloat16, device="cuda")   # H = 32: not a multiple of 64
+    kv = torch.zeros((8, 576), dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros((4, 32, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((4, 32), dtype=torch.float32, device="cuda")
+    idx = torch.zeros((4, 8), dtype=torch.int32, device="cuda")
+    ws = torch.empty(attn.attn_dsa_bwd_workspace_size(8, 576), dtype=torch.uint8, device="cuda")
+    with pytest.raises(attn.AttnError):
+        attn.attn_dsa_bwd(q, kv, o, o, lse, None, idx, None, torch.empty_like(q), torch.empty_like(kv), None, ws,
+                          0.1, False)
+    assert attn.attn_last_launch_count() == 0
