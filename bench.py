@@ -438,6 +438,112 @@ DECODE_SWEEP = [
 ]
 
 
+# Sparse top-k attention backward with shared latent key/value rows: the shapes of the
+# cudnn-frontend DSA backward pull request's tables (seqlen 4096, BF16, d_v 512, sink on,
+# every row's top-k length = topk).
+DSA_SWEEP = [
+    # s_q = s_kv, H, d_qk, topk
+    (4096, 64, 512, 128), (4096, 64, 512, 512), (4096, 64, 512, 2048),
+    (4096, 128, 512, 2048),
+    (4096, 128, 576, 128), (4096, 128, 576, 512), (4096, 128, 576, 2048),
+    (4096, 64, 576, 2048),
+]
+
+
+def dsa_prepare(s_q, s_kv, H, d_qk, topk, causal, seed=17):
+    """Synthetic inputs of the sparse top-k backward on the GPU: q, kv, dO ~ N(0, 1) bf16,
+    sink ~ N(0, 1), each row's list = topk distinct random keys (keys 0..i when causal,
+    padded with -1), and the forward's O (bf16) and L (FP32) from a plain PyTorch FP32
+    computation over the gathered keys (input preparation, not timed)."""
+    import torch
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    d_v = 512
+    q = torch.randn((s_q, H, d_qk), generator=g, device=dev).to(torch.bfloat16)
+    kv = torch.randn((s_kv, d_qk), generator=g, device=dev).to(torch.bfloat16)
+    do = torch.randn((s_q, H, d_v), generator=g, device=dev).to(torch.bfloat16)
+    sink = torch.randn((H,), generator=g, device=dev)
+    idx = torch.empty((s_q, topk), dtype=torch.int32, device=dev)
+    lens = torch.empty((s_q,), dtype=torch.int32, device=dev)
+    for r0 in range(0, s_q, 512):
+        r1 = min(s_q, r0 + 512)
+        keys = torch.rand((r1 - r0, s_kv), generator=g, device=dev)
+        rows = torch.arange(r0, r1, device=dev)[:, None]
+        if causal:
+            keys = torch.where(torch.arange(s_kv, device=dev)[None, :] <= rows, keys, torch.full_like(keys, 2.0))
+        order = keys.argsort(dim=1)[:, :topk].to(torch.int32)
+        n = torch.clamp(rows[:, 0] + 1, max=min(topk, s_kv)) if causal else torch.full((r1 - r0,), min(topk, s_kv),
+                                                                                     device=dev)
+        pos = torch.arange(topk, device=dev)[None, :]
+        idx[r0:r1] = torch.where(pos < n[:, None], order, torch.full_like(order, -1))
+        lens[r0:r1] = n.to(torch.int32)
+    o = torch.empty((s_q, H, d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((s_q, H), dtype=torch.float32, device=dev)
+    scale = d_qk ** -0.5
+    kvf = kv.float()
+    for r0 in range(0, s_q, 64):
+        r1 = min(s_q, r0 + 64)
+        ix = idx[r0:r1].long()
+        valid = ix >= 0
+        K = kvf[ix.clamp(min=0)]                                   # [r, topk, d_qk]
+        S = torch.einsum("rhd,rkd->rhk", q[r0:r1].float(), K) * scale
+        S = S.masked_fill(~valid[:, None, :], float("-inf"))
+        allS = torch.cat([S, sink[None, :, None].expand(r1 - r0, H, 1)], dim=2)
+        L = torch.logsumexp(allS, dim=2)
+        P = torch.exp(S - L[:, :, None])
+        o[r0:r1] = torch.einsum("rhk,rkd->rhd", P, K[:, :, :d_v]).to(torch.bfloat16)
+        lse[r0:r1] = L
+    return dict(q=q, kv=kv, do=do, sink=sink, idx=idx, lens=lens, o=o, lse=lse, scale=scale)
+
+
+def dsa_flops(s_q, H, d_qk, topk, d_v=512):
+    """2 s_q H topk (3 d_qk + 2 d_v): S, dP, dQ, dK, dV over every listed key."""
+    return 2.0 * s_q * H * topk * (3 * d_qk + 2 * d_v)
+
+
+def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=True):
+    """Time attn_dsa_bwd (its memsets and both kernels) with CUDA events; one JSON line with
+    TFLOPS by dsa_flops and the fraction of the measured dense BF16 peak."""
+    import torch
+
+    if build:
+        import __graft_entry__
+        __graft_entry__.build()
+    import exact_attention_flashattention_gb300 as attn
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    x = dsa_prepare(s_q, s_kv, H, d_qk, topk, causal)
+    dq = torch.empty_like(x["q"])
+    dkv = torch.empty_like(x["kv"])
+    dsink = torch.empty_like(x["sink"])
+    ws = torch.empty(attn.attn_dsa_bwd_workspace_size(s_kv, d_qk), dtype=torch.uint8, device=dev)
+
+    def call():
+        attn.attn_dsa_bwd(x["q"], x["kv"], x["o"], x["do"], x["lse"], x["sink"], x["idx"], x["lens"], dq, dkv, dsink,
+                          ws, x["scale"], causal, stream)
+
+    for _ in range(warmup):
+        call()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(iters):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / iters
+    if attn.attn_last_device_error(stream) != 0:
+        raise RuntimeError("device error word set")
+    tf = dsa_flops(s_q, H, d_qk, topk) / ms / 1e9
+    print(json.dumps({"sweep": f"dsa bwd s={s_q} H={H} QK={d_qk} V=512 topk={topk}" + (" causal" if causal else ""),
+                      "dtype": "bf16", "ms": ms, "tflops": tf, "pct_peak": 100 * tf / peak,
+                      "peak_basis": f"dense BF16 {peak} TFLOPS ({src})"}), flush=True)
+    return 0
+
+
 def run_sweep(iters=20):
     """Forward and backward TFLOPS of every workload of the list (CUDA events,
     3 warm-up calls, `iters` timed calls each).  One JSON line per workload;
@@ -534,6 +640,8 @@ def run_sweep(iters=20):
         del q, k, v, do, o, lse, dq, dk, dv, ws
     for name, B, Hq, Hkv, N, d in DECODE_SWEEP:
         run_decode(name, B, Hq, Hkv, N, d, iters=iters, warmup=3, build=False)
+    for s, H, d_qk, topk in DSA_SWEEP:
+        run_dsa(s, s, H, d_qk, topk, iters=iters, warmup=3, build=False)
     return 0
 
 
@@ -588,6 +696,8 @@ def main():
                     help="print fwd / bwd TFLOPS of every workload of the list instead of the bench line")
     ap.add_argument("--shape", default=None,
                     help="B,H,N,d[,noncausal] instead of the default workload (smaller cases for profiling)")
+    ap.add_argument("--dsa-shape", default=None,
+                    help="s_q,s_kv,H,d_qk,topk[,causal]: time the sparse top-k backward on that shape")
     ap.add_argument("--decode-shape", default=None,
                     help="B,Hq,Hkv,N,d: time decode on that cache (--steps timed calls, --warmup untimed)")
     args = ap.parse_args()
@@ -606,6 +716,11 @@ def main():
         B, Hq, Hkv, N, d = (int(x) for x in args.decode_shape.split(","))
         return run_decode(f"decode B={B} Hq={Hq} Hkv={Hkv} N={N} d={d}", B, Hq, Hkv, N, d, iters=args.steps,
                           warmup=args.warmup)
+    if args.dsa_shape:
+        parts = args.dsa_shape.split(",")
+        s_q, s_kv, H, d_qk, topk = (int(x) for x in parts[:5])
+        return run_dsa(s_q, s_kv, H, d_qk, topk, causal=len(parts) > 5 and parts[5] == "causal", iters=args.steps,
+                       warmup=args.warmup)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -128,3 +128,58 @@ def test_dsa_bwd_argument_errors(attn):
         attn.attn_dsa_bwd(q, kv, o, o, lse, None, idx, None, torch.empty_like(q), torch.empty_like(kv), None, ws,
                           0.1, False)
     assert attn.attn_last_launch_count() == 0
+
+
+def _sub_bwd(x, rows, idx_rows, scale, causal):
+    """The oracle backward of `rows` only (their own lists), inputs taken from the device."""
+    t = lambda a: a.float().cpu().numpy().astype(np.float64)
+    sel = torch.as_tensor(rows, device="cuda")
+    return oracle.dsa_bwd(t(x["q"][sel]), t(x["kv"]), t(x["o"][sel]), t(x["do"][sel]), t(x["lse"][sel]),
+                          t(x["sink"]), idx_rows, None, scale, causal, 512)
+
+
+def test_dsa_bwd_full_size_sampled(attn):
+    """s_q = s_kv = 4096, H = 128, QK 576, top-k 2048 (the largest shape of the pull
+    request's table), sink on, launched as bench.py times it.  dQ on sampled queries;
+    dKV on sampled keys (L is an input, so each listed (query, key) entry contributes on
+    its own: the oracle runs on the queries that list the key, each with that one entry);
+    dSink over all rows, 256 at a time."""
+    from bench import dsa_prepare
+    s, H, d_qk, topk = 4096, 128, 576, 2048
+    x = dsa_prepare(s, s, H, d_qk, topk, False)
+    scale = x["scale"]
+    dq = torch.full_like(x["q"], float("nan"))
+    dkv = torch.full_like(x["kv"], float("nan"))
+    dsink = torch.full_like(x["sink"], float("nan"))
+    ws = torch.empty(attn.attn_dsa_bwd_workspace_size(s, d_qk), dtype=torch.uint8, device="cuda")
+    attn.attn_dsa_bwd(x["q"], x["kv"], x["o"], x["do"], x["lse"], x["sink"], x["idx"], x["lens"], dq, dkv, dsink, ws,
+                      scale, False)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dkv.float()).all()
+    idx = x["idx"].cpu().numpy()
+    rng = np.random.default_rng(3)
+
+    rows = [0, 1, 2047, s - 1] + [int(r) for r in rng.integers(0, s, 4)]
+    ref = _sub_bwd(x, rows, idx[rows], scale, False)
+    got = dq[torch.as_tensor(rows, device="cuda")].float().cpu().numpy().astype(np.float64)
+    for n, r in enumerate(rows):
+        assert rel_fro(got[n], ref["dq"][n]) <= TOL_GRAD_RELFRO, ("dq", r)
+
+    keys = [0, s - 1] + [int(k) for k in rng.integers(0, s, 2)]
+    got_kv = dkv.float().cpu().numpy().astype(np.float64)
+    for j in keys:
+        q_rows = np.nonzero((idx == j).any(axis=1))[0]
+        assert np.all((idx[q_rows] == j).sum(axis=1) == 1)  # the lists hold distinct keys
+        ref_j = np.zeros(d_qk)
+        for c0 in range(0, len(q_rows), 256):
+            part = q_rows[c0:c0 + 256]
+            one = np.full((len(part), 1), j, dtype=np.int32)
+            ref_j += _sub_bwd(x, part.tolist(), one, scale, False)["dkv"][j]
+        assert rel_fro(got_kv[j], ref_j) <= TOL_GRAD_RELFRO, ("dkv", j)
+
+    dsink_ref = np.zeros(H)
+    empty = np.full((256, 1), -1, dtype=np.int32)
+    for r0 in range(0, s, 256):
+        dsink_ref += _sub_bwd(x, list(range(r0, r0 + 256)), empty, scale, False)["dsink"]
+    assert rel_fro(dsink.cpu().numpy().astype(np.float64), dsink_ref) <= TOL_DSINK
