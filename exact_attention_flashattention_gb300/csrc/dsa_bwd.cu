@@ -9,11 +9,12 @@
 //   dP^T = V dO^T       [keys x heads]  (the first 512 columns of the same chunks)
 //   P^T = exp(S^T - L), dS^T = scale P^T (dP^T - D)        (elementwise warpgroup)
 //   dQ^T += K^T dS^T    [d_qk x heads]  (d on the lanes, 128 rows per product)
-//   dKV_tile = dS^T Q + [P^T dO, 0]     [keys x d_qk], 64 columns at a time, added to
-//                                        the FP32 accumulator with vector reductions
+//   dKV_tile = dS^T Q + [P^T dO, 0]     [keys x d_qk], 64 columns at a time (A = dS^T,
+//                                        P^T from TMEM), added to the FP32 accumulator
+//                                        with vector reductions of whole 128-byte pieces
 // TMEM (512 columns): S^T 0..63 (P^T packed to 16 bits over its first 32 columns),
 // dP^T 64..127, dQ^T 128..447 (five 64-column blocks at d_qk = 576, four at 512),
-// dKV chunk 448..511.  Shared memory: Q and dO of the 64 heads (72 + 64 KB), a ring of
+// dKV chunk 448..511; dS^T packed to 16 bits over dP^T's first 32 columns.  Shared memory: Q and dO of the 64 heads (72 + 64 KB), a ring of
 // four 16 KB key chunks (128 keys x 64 columns, gathered by a loader warpgroup with
 // cp.async), and dS^T (16 KB).  The key chunks are gathered twice per tile: for S^T /
 // dP^T, and again, two at a time, for dQ^T (the whole 128 x 576 tile does not fit
@@ -58,7 +59,8 @@ struct DsaLayout {
     static constexpr int kBarDkvFree = 12;
     static constexpr int kBarDqFull = 13;
     static constexpr int kBarTeardown = 14;
-    static constexpr int kNumBars = 15;
+    static constexpr int kBarDqDone = 15;    // the tile's dQ^T products have read dS^T in shared memory
+    static constexpr int kNumBars = 16;
     static_assert(8 * kNumBars <= 8 * 16, "barrier area");
     static constexpr int kL2eOff = kAux + 8 * 16;       // float [64]: L log2 e
     static constexpr int kDOff = kL2eOff + 4 * 64;      // float [64]: D = dO . O
@@ -137,6 +139,7 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(&bars[L::kBarDkvFree], 128);
         mbar_init(&bars[L::kBarDqFull], 1);
         mbar_init(&bars[L::kBarTeardown], 1);
+        mbar_init(&bars[L::kBarDqDone], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -190,8 +193,9 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             const int key = dsa_key(p, i, len, t * kDsaTile + r);
             if (!mbar_wait(&bars[L::kBarSFull], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
             tc_fence_after();
-            // Two halves of 32 heads.  P^T (16-bit pairs) goes over S^T's first 32 columns: half
-            // 0 writes columns 0-15 (heads 0-31, already in registers), half 1 columns 16-31.
+            // Two halves of 32 heads.  P^T (16-bit pairs) goes over S^T's first 32 columns and
+            // dS^T over dP^T's: half 0 writes columns 0-15 of each (heads 0-31, already in
+            // registers), half 1 columns 16-31.  dS^T also goes to shared memory for dQ^T.
 #pragma unroll 1
             for (int hf = 0; hf < 2; ++hf) {
                 uint32_t s[32], dp[32];
@@ -213,6 +217,7 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     dk[e >> 1] = bf16x2_bits(g0, g1);
                 }
                 tmem_st16(tmem + lane_base + L::kTmemS + 16 * hf, pk);
+                tmem_st16(tmem + lane_base + L::kTmemDP + 16 * hf, dk);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
@@ -224,26 +229,38 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             tc_fence_before();
             mbar_arrive(&bars[L::kBarPReady]);
 
-            // dKV of this tile, 64 columns at a time, into the FP32 accumulator.
-            float* dst = key >= 0 ? p.dkv_acc + (size_t)key * DQK : nullptr;
+            // dKV of this tile, 64 columns at a time, into the FP32 accumulator.  Each warp turns
+            // its 32 rows (thread = key) around in shared memory (dS^T's buffer, free once the
+            // tile's dQ^T products have read it), so that one reduction instruction covers four
+            // whole 128-byte row pieces instead of 32 scattered 16-byte ones.
+            if (!mbar_wait(&bars[L::kBarDqDone], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+            uint8_t* stage = smem + L::kDS + warp * 4096;     // 32 rows x 128 bytes
+            const int lane = r & 31;
             for (int cc = 0; cc < L::kNC; ++cc, ++j) {
                 if (!mbar_wait(&bars[L::kBarDkvFull], j & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
                 tc_fence_after();
-                uint32_t v[32], w[32];
-                tmem_ld32(tmem + lane_base + L::kTmemDKV, v);
-                tmem_ld32(tmem + lane_base + L::kTmemDKV + 32, w);
+                uint32_t v[2][32];
+                tmem_ld32(tmem + lane_base + L::kTmemDKV, v[0]);
+                tmem_ld32(tmem + lane_base + L::kTmemDKV + 32, v[1]);
                 tmem_wait_ld();
                 tc_fence_before();
                 mbar_arrive(&bars[L::kBarDkvFree]);
-                if (dst) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_v4(dst + cc * 64 + e, __uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                   __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3]));
+                for (int hf = 0; hf < 2; ++hf) {
 #pragma unroll
-                    for (int e = 0; e < 32; e += 4)
-                        red_add_v4(dst + cc * 64 + 32 + e, __uint_as_float(w[e]), __uint_as_float(w[e + 1]),
-                                   __uint_as_float(w[e + 2]), __uint_as_float(w[e + 3]));
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<uint4*>(stage + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                            make_uint4(v[hf][4 * c], v[hf][4 * c + 1], v[hf][4 * c + 2], v[hf][4 * c + 3]);
+                    __syncwarp();
+#pragma unroll
+                    for (int it = 0; it < 8; ++it) {
+                        const int row = 4 * it + (lane >> 3), piece = lane & 7;
+                        const int krow = __shfl_sync(0xffffffffu, key, row);
+                        const float4 f = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) << 4));
+                        if (krow >= 0)
+                            red_add_v4(p.dkv_acc + (size_t)krow * DQK + cc * 64 + 32 * hf + 4 * piece, f.x, f.y, f.z, f.w);
+                    }
+                    __syncwarp();
                 }
             }
         }
@@ -329,13 +346,14 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 warp_mma_commit(&bars[L::kBarKEmpty + slot + 1]);
             }
             if (!ok) break;
+            warp_mma_commit(&bars[L::kBarDqDone]);
             // dKV chunk cc = dS^T Q[:, cc] (+ P^T dO[:, cc]), flushed by the elementwise warps
             for (int cc = 0; cc < L::kNC; ++cc, ++j) {
                 if (!warp_mbar_wait(&bars[L::kBarDkvFree], (j & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    warp_mma_ss(tmem + L::kTmemDKV, sdesc_sw128(ds_base + kk * 32, 16, 1024),
+                    warp_mma_ts(tmem + L::kTmemDKV, tmem + L::kTmemDP + 8 * kk,
                                 sdesc_sw128(q_base + cc * L::kPanel + kk * 2048, L::kPanel, 1024), kIdKV, kk != 0);
                 if (cc < L::kNV) {
 #pragma unroll
