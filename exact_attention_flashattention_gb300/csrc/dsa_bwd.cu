@@ -368,8 +368,10 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         warp_mma_commit(&bars[L::kBarTeardown]);
         mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
     } else {
-        // ------------------------------------------------ gather loaders (thread = key of the tile)
+        // ------------------------------------------------ gather loaders: eight consecutive threads
+        // copy one 128-byte row piece, so a warp's copies cover four whole rows (lines)
         const int r = threadIdx.x - 160;
+        const int piece = r & 7, row0 = r >> 3;   // rows row0 + 16 j, j = 0..7
         if (r == 0 && n_tiles > 0) {
             mbar_arrive_expect_tx(&bars[L::kBarQFull], (L::kNC + L::kNV) * L::kPanel);
             const int y = i * p.H + h0;
@@ -381,9 +383,12 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bool ok = true;
         uint32_t k = 0;
         for (int t = 0; t < n_tiles && ok; ++t) {
-            const int key = dsa_key(p, i, len, t * kDsaTile + r);
-            const uint16_t* src_row = p.kv + (key >= 0 ? (size_t)key * DQK : 0);
-            const uint32_t nbytes = key >= 0 ? 16u : 0u;
+            uint32_t src_off[8];   // element offset of the row (0 for masked entries) | valid bit 31
+#pragma unroll
+            for (int jj = 0; jj < 8; ++jj) {
+                const int key = dsa_key(p, i, len, t * kDsaTile + row0 + 16 * jj);
+                src_off[jj] = key >= 0 ? ((uint32_t)key * DQK) | 0x80000000u : 0u;
+            }
             for (int pass = 0; pass < 2 && ok; ++pass) {
                 for (int c = 0; c < L::kNCE; ++c, ++k) {
                     const uint32_t slot = k & 3;
@@ -394,8 +399,11 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (c < L::kNC) {
                         const uint32_t dst = ring + slot * L::kChunk;
 #pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            cp_async_16(dst + sw128_offset(r, q), src_row + 64 * c + 8 * q, nbytes);
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const uint32_t off = src_off[jj] & 0x7FFFFFFFu;
+                            cp_async_16(dst + sw128_offset(row0 + 16 * jj, piece), p.kv + off + 64 * c + 8 * piece,
+                                        (src_off[jj] >> 31) ? 16u : 0u);
+                        }
                     }
                     cp_async_commit();
                     // Entry k - 2 has landed (two entries stay in flight): publish it.
