@@ -236,6 +236,12 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             if (!mbar_wait(&bars[L::kBarDqDone], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
             uint8_t* stage = smem + L::kDS + warp * 4096;     // 32 rows x 128 bytes
             const int lane = r & 31;
+            float* rdst[8];   // rows 4 it + lane / 8 of this warp: their accumulator rows + piece offset
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+                const int krow = __shfl_sync(0xffffffffu, key, 4 * it + (lane >> 3));
+                rdst[it] = krow >= 0 ? p.dkv_acc + (size_t)krow * DQK + 4 * (lane & 7) : nullptr;
+            }
             for (int cc = 0; cc < L::kNC; ++cc, ++j) {
                 if (!mbar_wait(&bars[L::kBarDkvFull], j & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
                 tc_fence_after();
@@ -255,10 +261,9 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
 #pragma unroll
                     for (int it = 0; it < 8; ++it) {
                         const int row = 4 * it + (lane >> 3), piece = lane & 7;
-                        const int krow = __shfl_sync(0xffffffffu, key, row);
                         const float4 f = *reinterpret_cast<const float4*>(stage + row * 128 + ((piece ^ (row & 7)) << 4));
-                        if (krow >= 0)
-                            red_add_v4(p.dkv_acc + (size_t)krow * DQK + cc * 64 + 32 * hf + 4 * piece, f.x, f.y, f.z, f.w);
+                        if (rdst[it] != nullptr)
+                            red_add_v4(rdst[it] + cc * 64 + 32 * hf, f.x, f.y, f.z, f.w);
                     }
                     __syncwarp();
                 }
