@@ -15,14 +15,16 @@
 // TMEM (512 columns): S^T 0..63 (P^T packed to 16 bits over its first 32 columns),
 // dP^T 64..127, dQ^T 128..447 (five 64-column blocks at d_qk = 576, four at 512),
 // dKV chunk 448..511; dS^T packed to 16 bits over dP^T's first 32 columns.  Shared memory: Q and dO of the 64 heads (72 + 64 KB), a ring of
-// four 16 KB key chunks (128 keys x 64 columns, gathered by a loader warpgroup with
+// four 16 KB key chunks (128 keys x 64 columns, gathered by eight loader warps with
 // cp.async), and dS^T (16 KB).  The key chunks are gathered twice per tile: for S^T /
 // dP^T, and again, two at a time, for dQ^T (the whole 128 x 576 tile does not fit
 // beside Q and dO).
 //
-// Roles (288 threads): warps 0-3 elementwise + dKV flush + dQ epilogue (thread = TMEM
-// lane = key of the tile, then = d row of dQ^T); warp 4 issues the MMAs (whole warp,
-// lane 0 issues); warps 5-8 gather key chunks (thread = key) and, thread 160, load Q / dO.
+// Roles (512 threads, registers split with setmaxnreg): warps 0-3 elementwise + dKV flush +
+// dQ epilogue (thread = TMEM lane = key of the tile, then = d row of dQ^T); warp 4 issues the
+// MMAs (whole warp, lane 0 issues); warps 8-15 gather key chunks and, thread 256, load Q / dO.
+// More gathering threads keep more copies issued (four loader warps: 14.1 ms, two: 15.5 ms,
+// eight: 13.6 ms at H = 128, QK 576, top-k 2048).
 #include <cuda_bf16.h>
 
 #include "attn_internal.h"
@@ -31,7 +33,7 @@
 namespace gb300 {
 namespace {
 
-constexpr int kDsaThreads = 288;
+constexpr int kDsaThreads = 512;
 constexpr int kDsaHeads = 64;     // heads per CTA
 constexpr int kDsaTile = 128;     // list entries (keys) per tile
 constexpr int kDsaDv = 512;
@@ -130,7 +132,7 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     if (threadIdx.x == 0) {
         mbar_init(&bars[L::kBarQFull], 1);
         for (int s = 0; s < 4; ++s) {
-            mbar_init(&bars[L::kBarKFull + s], 128);
+            mbar_init(&bars[L::kBarKFull + s], 256);
             mbar_init(&bars[L::kBarKEmpty + s], 1);
         }
         mbar_init(&bars[L::kBarSFull], 1);
@@ -154,6 +156,7 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
     const WaitGuard guard{abort_flag, p.error, kWaitLimitNs};
 
     if (warp < 4) {
+        regs_inc<208>();   // 128 x 208 + 128 x 80 + 256 x 96 = 61440 of the 65536 launched
         // ------------------------------------------------ elementwise, dKV flush, dQ epilogue
         const int r = threadIdx.x;                          // TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -299,7 +302,9 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                 }
             }
         }
-    } else if (warp == 4) {
+    } else if (warp < 8) {
+      regs_dec<80>();
+      if (warp == 4) {
         // ------------------------------------------------ MMA issuer (the whole warp; lane 0 issues)
         constexpr uint32_t kIdS = idesc_f16(128, 64, true, false, false);    // S^T, dP^T
         constexpr uint32_t kIdQ = idesc_f16(128, 64, true, true, true);      // dQ^T = K^T dS^T
@@ -372,11 +377,13 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (ok && n_tiles > 0) warp_mma_commit(&bars[L::kBarDqFull]);
         warp_mma_commit(&bars[L::kBarTeardown]);
         mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
+      }
     } else {
+        regs_dec<96>();
         // ------------------------------------------------ gather loaders: eight consecutive threads
         // copy one 128-byte row piece, so a warp's copies cover four whole rows (lines)
-        const int r = threadIdx.x - 160;
-        const int piece = r & 7, row0 = r >> 3;   // rows row0 + 16 j, j = 0..7
+        const int r = threadIdx.x - 256;
+        const int piece = r & 7, row0 = r >> 3;   // rows row0 + 32 j, j = 0..3
         if (r == 0 && n_tiles > 0) {
             mbar_arrive_expect_tx(&bars[L::kBarQFull], (L::kNC + L::kNV) * L::kPanel);
             const int y = i * p.H + h0;
@@ -388,10 +395,10 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bool ok = true;
         uint32_t k = 0;
         for (int t = 0; t < n_tiles && ok; ++t) {
-            uint32_t src_off[8];   // element offset of the row (0 for masked entries) | valid bit 31
+            uint32_t src_off[4];
 #pragma unroll
-            for (int jj = 0; jj < 8; ++jj) {
-                const int key = dsa_key(p, i, len, t * kDsaTile + row0 + 16 * jj);
+            for (int jj = 0; jj < 4; ++jj) {
+                const int key = dsa_key(p, i, len, t * kDsaTile + row0 + 32 * jj);
                 src_off[jj] = key >= 0 ? ((uint32_t)key * DQK) | 0x80000000u : 0u;
             }
             for (int pass = 0; pass < 2 && ok; ++pass) {
@@ -404,9 +411,9 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     if (c < L::kNC) {
                         const uint32_t dst = ring + slot * L::kChunk;
 #pragma unroll
-                        for (int jj = 0; jj < 8; ++jj) {
+                        for (int jj = 0; jj < 4; ++jj) {
                             const uint32_t off = src_off[jj] & 0x7FFFFFFFu;
-                            cp_async_16(dst + sw128_offset(row0 + 16 * jj, piece), p.kv + off + 64 * c + 8 * piece,
+                            cp_async_16(dst + sw128_offset(row0 + 32 * jj, piece), p.kv + off + 64 * c + 8 * piece,
                                         (src_off[jj] >> 31) ? 16u : 0u);
                         }
                     }
