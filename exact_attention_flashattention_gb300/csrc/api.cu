@@ -344,6 +344,11 @@ attn_status_t bwd_common(int stage, const void* q, const void* k, const void* v,
     a.num_sms = di.sms;
     a.device = di.device;
     a.error = di.err_ptr;
+    a.sched = nullptr;
+    if (seq.cu && (stage < 0 || stage == 1)) {  // packed sequences: dynamic distribution
+        a.sched = take_sched_counter(di, static_cast<cudaStream_t>(stream));
+        if (!a.sched) return ATTN_ERR_CUDA;
+    }
     if (launch_bwd(a, static_cast<cudaStream_t>(stream), stage) != cudaSuccess) return ATTN_ERR_CUDA;
     t_last_launches = stage < 0 ? 3 : 1;
     return ATTN_OK;

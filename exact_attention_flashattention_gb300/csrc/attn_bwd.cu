@@ -141,8 +141,11 @@ struct BwdLayout {
     static constexpr int kBarSFull = 8, kBarDpFull = 9, kBarPReady = 10, kBarDsReady = 11;
     static constexpr int kBarDqFull = 12, kBarDqFree = 13, kBarDkvFull = 14, kBarDkvEmpty = 15;
     static constexpr int kBarTeardown = 16;
-    static constexpr int kNumBars = 17;
-    static constexpr int kMiscOff = kAux + kNumBars * 8;
+    static constexpr int kBarSchedFull = 17;    // [4] packed sequences: dynamic unit distribution
+    static constexpr int kBarSchedEmpty = 21;   // [4]
+    static constexpr int kNumBars = 25;
+    static constexpr int kSchedSlotWord = 2 * kNumBars;  // int index of the ring's 4 unit slots
+    static constexpr int kMiscOff = kAux + kNumBars * 8 + 16;
     static constexpr int kBytes = kMiscOff + 16;
     // TMEM columns: dV, dK accumulators; S^T (P^T packed over it); dP^T (dS^T packed over it),
     // reused for the dQ_i tile once dK has consumed dS^T.
@@ -184,13 +187,53 @@ __device__ __forceinline__ bool bwd_item(int u, int s, int T, int causal, const 
     return true;
 }
 
-template <int D, bool BF16, bool kTM>
+// Dynamic distribution for packed sequences of different lengths, as in the forward: one
+// thread takes units from the launch's counter and publishes them through a 4-entry ring in
+// the barrier area; every role reads the same sequence of units, holds an entry until its unit
+// is done, releases it with its own arrival, and the scheduler claims at most one unit ahead.
+// Consumers: the 256 elementwise threads, the 128 drain threads, the MMA warp and the TMA
+// thread.
+constexpr int kSchedDepth = 4;
+constexpr int kSchedAhead = 1;
+constexpr int kBwdSchedConsumers = 256 + 128 + 32 + 1;
+
+// This CTA's sequence of units; next() returns the next unit, or -1 at the end (or when a
+// wait gave up).  kDyn = false: blockIdx.x, blockIdx.x + gridDim.x, ...
+template <bool kDyn>
+struct BwdUnits;
+
+template <>
+struct BwdUnits<false> {
+    int u;
+    const int n_units;
+    __device__ explicit BwdUnits(int n) : u((int)blockIdx.x - (int)gridDim.x), n_units(n) {}
+    template <class L>
+    __device__ int next(uint64_t*, const WaitGuard&, int) {
+        u += (int)gridDim.x;
+        return u < n_units ? u : -1;
+    }
+};
+
+template <>
+struct BwdUnits<true> {
+    uint32_t k = 0;   // ring entries taken
+    __device__ explicit BwdUnits(int) {}
+    template <class L>
+    __device__ int next(uint64_t* bars, const WaitGuard& g, int code) {
+        const volatile int* ring = reinterpret_cast<volatile int*>(bars) + L::kSchedSlotWord;
+        if (k > 0) mbar_arrive(&bars[L::kBarSchedEmpty + (k - 1) % kSchedDepth]);
+        if (!mbar_wait(&bars[L::kBarSchedFull + k % kSchedDepth], (k / kSchedDepth) & 1, g, code)) return -1;
+        return ring[k++ % kSchedDepth];
+    }
+};
+
+template <int D, bool BF16, bool kTM, bool kDyn>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                 const float* __restrict__ nlse2, const float* __restrict__ ndelta, float* __restrict__ dq_acc,
                 void* __restrict__ dk_out, void* __restrict__ dv_out, const SeqDesc seq, float scale, int causal,
-                int smem_slack, int* error) {
+                int smem_slack, unsigned int* __restrict__ sched, int* error) {
     using L = BwdLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -212,7 +255,13 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int n_units = seq.B * seq.H * bwd_units_per_head(T, causal);
 
     if (threadIdx.x == 0) {
-        for (int b = 0; b < L::kNumBars; ++b) mbar_init(&bars[b], 1);
+        for (int b = 0; b < L::kBarSchedFull; ++b) mbar_init(&bars[b], 1);
+        if (kDyn) {
+            for (int b = 0; b < kSchedDepth; ++b) {
+                mbar_init(&bars[L::kBarSchedFull + b], 1);
+                mbar_init(&bars[L::kBarSchedEmpty + b], kBwdSchedConsumers);
+            }
+        }
         mbar_init(&bars[L::kBarPReady], 256);
         mbar_init(&bars[L::kBarDsReady], 256);
         mbar_init(&bars[L::kBarDqFree], 128);
@@ -250,7 +299,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const uint64_t sc2 = f2_pack(scale, scale);
         uint32_t g = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        BwdUnits<kDyn> units(n_units);
+        for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutSoftmax)) >= 0;) {
             for (int sidx = 0; sidx < 2 && ok; ++sidx) {
                 BwdItem w;
                 if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
@@ -344,7 +394,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t g = 0;
         int k = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        BwdUnits<kDyn> units(n_units);
+        for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutCorr)) >= 0;) {
             for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                 BwdItem w;
                 if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
@@ -441,7 +492,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 }
                 warp_mma_commit(&bars[L::kBarDqFull]);
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            BwdUnits<kDyn> units(n_units);
+            for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutMma)) >= 0;) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
                     if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
@@ -507,6 +559,20 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
             warp_mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
+        } else if (kDyn && warp == 15 && lane == 0) {
+            // ------------------------------------------------------ scheduler (packed sequences)
+            for (uint32_t k = 0;; ++k) {
+                const uint32_t pos = k % kSchedDepth, e = k - 1 - kSchedAhead;  // e: entry to be released
+                if (k > (uint32_t)kSchedAhead &&
+                    !mbar_wait_sleep(&bars[L::kBarSchedEmpty + e % kSchedDepth], (e / kSchedDepth) & 1, guard,
+                                     kDevTimeoutLoad))
+                    break;
+                const unsigned int u = atomicAdd(sched, 1u);
+                const int val = u < (unsigned int)n_units ? (int)u : -1;
+                reinterpret_cast<volatile int*>(bars)[L::kSchedSlotWord + pos] = val;
+                mbar_arrive(&bars[L::kBarSchedFull + pos]);  // release: the slot is written first
+                if (val < 0) break;
+            }
         } else if (warp == 13 && lane == 0) {
             // ------------------------------------------------------ TMA producer
             uint32_t g = 0;
@@ -531,7 +597,8 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 ++g;
                 return true;
             };
-            for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+            BwdUnits<kDyn> units(n_units);
+            for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutLoad)) >= 0;) {
                 for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
                     BwdItem w;
                     if (!bwd_item<kTM>(u, sidx, T, causal, seq, w)) break;
@@ -597,13 +664,18 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         const int smem_bytes = want < max_smem ? want : max_smem;
         const int slack = smem_bytes - L::kBytes;
         if (slack < 0) return cudaErrorInvalidConfiguration;
-        auto kern = attn_bwd_kernel<D, BF16, kTM>;
+        // Packed sequences of different lengths take units from the launch's counter; the
+        // fixed-length layouts keep the static split (their units all carry the same work).
+        auto kern = attn_bwd_kernel<D, BF16, kTM, false>;
+        if constexpr (kTM) {
+            if (a.seq.cu != nullptr) kern = attn_bwd_kernel<D, BF16, kTM, true>;
+        }
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
         if (e != cudaSuccess) return e;
         const long n_units = (long)a.BH * (a.causal ? (T + 1) / 2 : T);
         const int grid = (int)(n_units < a.num_sms ? n_units : a.num_sms);
         kern<<<grid, kThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.tm_do, a.lse2, a.delta, a.dq_acc,
-                                                      a.dk, a.dv, a.seq, a.scale, a.causal, slack, a.error);
+                                                      a.dk, a.dv, a.seq, a.scale, a.causal, slack, a.sched, a.error);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -61,6 +61,7 @@ struct BwdArgs {
     float* dq_acc;    // [ws_rows, d] FP32
     long ws_rows;
     SeqDesc seq;
+    unsigned int* sched;  // packed sequences: work counter of the main kernel's launch, zero at launch
     int BH, N, d;
     float scale;
     int causal;
