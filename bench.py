@@ -497,9 +497,12 @@ def dsa_prepare(s_q, s_kv, H, d_qk, topk, causal, seed=17):
     return dict(q=q, kv=kv, do=do, sink=sink, idx=idx, lens=lens, o=o, lse=lse, scale=scale)
 
 
-def dsa_flops(s_q, H, d_qk, topk, d_v=512):
-    """2 s_q H topk (3 d_qk + 2 d_v): S, dP, dQ, dK, dV over every listed key."""
-    return 2.0 * s_q * H * topk * (3 * d_qk + 2 * d_v)
+def dsa_flops(s_q, H, d_qk, topk, d_v=512, entries=None):
+    """2 s_q H topk (3 d_qk + 2 d_v): S, dP, dQ, dK, dV over every listed key (the pull
+    request's formula).  `entries`: the number of valid list entries over all rows, when rows
+    are shorter than topk (causal lists), in place of s_q topk."""
+    n = s_q * topk if entries is None else entries
+    return 2.0 * n * H * (3 * d_qk + 2 * d_v)
 
 
 def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=True):
@@ -537,7 +540,7 @@ def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=Tr
     ms = a.elapsed_time(b) / iters
     if attn.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error word set")
-    tf = dsa_flops(s_q, H, d_qk, topk) / ms / 1e9
+    tf = dsa_flops(s_q, H, d_qk, topk, entries=int(x["lens"].sum().item())) / ms / 1e9
     print(json.dumps({"sweep": f"dsa bwd s={s_q} H={H} QK={d_qk} V=512 topk={topk}" + (" causal" if causal else ""),
                       "dtype": "bf16", "ms": ms, "tflops": tf, "pct_peak": 100 * tf / peak,
                       "peak_basis": f"dense BF16 {peak} TFLOPS ({src})"}), flush=True)
