@@ -160,32 +160,45 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         // ------------------------------------------------ elementwise, dKV flush, dQ epilogue
         const int r = threadIdx.x;                          // TMEM lane
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        // D = dO . O and L log2 e for the 64 heads (two threads per head), and the sink gradient.
+        // D = dO . O and L log2 e for the 64 heads, and the sink gradient.  Warp w takes heads
+        // 16 w .. 16 w + 15, one row at a time: each load instruction covers 512 contiguous bytes.
         {
-            const int h = r >> 1, half = r & 1;
-            const size_t row = (size_t)i * p.H + h0 + h;
-            const uint4* o4 = reinterpret_cast<const uint4*>(p.o + row * kDsaDv + 256 * half);
-            const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + row * kDsaDv + 256 * half);
-            float acc = 0.f;
-#pragma unroll 4
-            for (int c = 0; c < 32; ++c) {
-                const uint4 a = __ldg(o4 + c), b = __ldg(d4 + c);
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+            const int lane = r & 31;
+#pragma unroll 1
+            for (int hh = 0; hh < 16; hh += 4) {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
-                    const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
-                    acc = fmaf(fa.x, fb.x, acc);
-                    acc = fmaf(fa.y, fb.y, acc);
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    const size_t row = (size_t)i * p.H + h0 + 16 * warp + hh + q4;
+                    const uint4* o4 = reinterpret_cast<const uint4*>(p.o + row * kDsaDv);
+                    const uint4* d4 = reinterpret_cast<const uint4*>(p.dout + row * kDsaDv);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const uint4 a = __ldg(o4 + 32 * c + lane), b = __ldg(d4 + 32 * c + lane);
+                        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&aw[e]));
+                            const float2 fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bw[e]));
+                            acc[q4] = fmaf(fa.x, fb.x, acc[q4]);
+                            acc[q4] = fmaf(fa.y, fb.y, acc[q4]);
+                        }
+                    }
                 }
-            }
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            if (half == 0) {
-                const float lse = __ldg(p.lse + row);
-                d_s[h] = acc;
-                l2e_s[h] = lse * kLog2e;
-                if (p.sink != nullptr && p.dsink != nullptr && lse > -INFINITY)
-                    atomicAdd(p.dsink + h0 + h, -expf(__ldg(p.sink + h0 + h) - lse) * acc);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) acc[q4] += __shfl_xor_sync(0xffffffffu, acc[q4], o);
+                }
+                if (lane < 4) {
+                    const int h = 16 * warp + hh + lane;
+                    const float dsum = lane == 0 ? acc[0] : lane == 1 ? acc[1] : lane == 2 ? acc[2] : acc[3];
+                    const float lse = __ldg(p.lse + (size_t)i * p.H + h0 + h);
+                    d_s[h] = dsum;
+                    l2e_s[h] = lse * kLog2e;
+                    if (p.sink != nullptr && p.dsink != nullptr && lse > -INFINITY)
+                        atomicAdd(p.dsink + h0 + h, -expf(__ldg(p.sink + h0 + h) - lse) * dsum);
+                }
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
         }
