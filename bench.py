@@ -55,13 +55,17 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+# The sources the attention forward / backward kernels are compiled from (the other kernels of
+# the library do not change their DRAM traffic).
+ATTN_KERNEL_SOURCES = ("attn_bwd.cu", "attn_fwd.cu", "attn_internal.h", "ptx.cuh", "seq.cuh")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "exact_attention_flashattention_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in ATTN_KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()[:16]
 
 
