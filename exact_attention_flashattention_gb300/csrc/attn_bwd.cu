@@ -388,7 +388,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     } else if (warp < 12) {
         // ------------------------------------------------------ dQ drain, dK/dV epilogue
         // d = 128 holds a whole 128-column dQ^T tile in registers; d = 64 needs fewer.
-        if constexpr (D == 128) regs_inc<144>(); else regs_dec<112>();
+        if constexpr (D == 128) regs_inc<136>(); else regs_dec<112>();
         const int row = (warp & 3) * 32 + lane;
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         uint32_t g = 0;
@@ -464,9 +464,9 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             }
         }
     } else {
-        // warps 12-15; the split 2 x 144 + 144 + 80 (d = 128) or 2 x 144 + 112 + 112 (d = 64)
+        // warps 12-15; the split 2 x 144 + 136 + 88 (d = 128) or 2 x 144 + 112 + 112 (d = 64)
         // uses exactly the 65536 registers the block is launched with
-        if constexpr (D == 128) regs_dec<80>(); else regs_dec<112>();
+        if constexpr (D == 128) regs_dec<88>(); else regs_dec<112>();
         if (warp == 12) {
             // ------------------------------------------------------ MMA issuer (the whole warp; lane 0 issues)
             constexpr uint32_t kIdescS = idesc_f16(128, 128, BF16, false, false);   // S^T, dP^T
@@ -500,19 +500,32 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     if (!warp_mbar_wait(&bars[L::kBarKFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     if (!warp_mbar_wait(&bars[L::kBarVFull], k & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                     tc_fence_after();
-                    for (int it = 0; it < w.n; ++it, ++g) {
-                        const uint32_t st = g & 1;
-                        const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
-                        if (!warp_mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                    // S^T = K_j Q_i^T into the S columns (last read by the previous dV, issued earlier)
+                    auto issue_s = [&](uint32_t gg) -> bool {
+                        const uint32_t sst = gg & 1;
+                        if (!warp_mbar_wait(&bars[L::kBarQFull + sst], (gg >> 1) & 1, guard, kDevTimeoutMma)) return false;
                         tc_fence_after();
-                        // S^T = K_j Q_i^T (its TMEM columns were last read by the previous dV, issued earlier)
+                        const uint32_t sqs = q_base + sst * L::kTile;
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
                             warp_mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024),
-                                   sdesc_sw128(qs + off, 16, 1024), kIdescS, kk > 0);
+                                   sdesc_sw128(sqs + off, 16, 1024), kIdescS, kk > 0);
                         }
                         warp_mma_commit(&bars[L::kBarSFull]);
+                        return true;
+                    };
+                    for (int it = 0; it < w.n; ++it, ++g) {
+                        const uint32_t st = g & 1;
+                        const uint32_t qs = q_base + st * L::kTile, dos = do_base + st * L::kTile;
+                        // d = 128: S^T of query tile i was issued after dV of tile i - 1 (below), so
+                        // the elementwise warps can start its P^T while dK and dQ^T of i - 1 run.
+                        if (kDqAfterS || it == 0) {
+                            if (!issue_s(g)) { ok = false; break; }
+                        } else {
+                            if (!warp_mbar_wait(&bars[L::kBarQFull + st], (g >> 1) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
+                            tc_fence_after();
+                        }
                         // d = 64: the previous query tile's dQ goes between S^T and dP^T, so the
                         // elementwise P^T pass overlaps it as well as dP^T.  d = 128: it stays at the
                         // end of the previous tile, where S^T hides the longer drain of its reductions
@@ -539,6 +552,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             warp_mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol,
                                    sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
                         }
+                        if (!kDqAfterS && it + 1 < w.n && !issue_s(g + 1)) { ok = false; break; }
                         // dK += dS^T Q_i
                         if (!warp_mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
