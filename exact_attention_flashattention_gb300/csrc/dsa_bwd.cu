@@ -51,7 +51,12 @@ struct DsaLayout {
     static constexpr int kDO = kQ + kNC * kPanel;
     static constexpr int kRing = kDO + kNV * kPanel;
     static constexpr int kDS = kRing + 4 * kChunk;
-    static constexpr int kAux = kDS + kChunk;
+    // QK = 512: dQ^T needs four TMEM blocks, which leaves 64 columns for P^T and dS^T of a tile
+    // and room in shared memory for a separate flush staging buffer, so a tile's dKV products
+    // and flush can run under the next tile's gathers (kOvl).
+    static constexpr bool kOvl = (DQK == 512);
+    static constexpr int kStage = kDS + kChunk;         // kOvl: 16 KB flush staging
+    static constexpr int kAux = kStage + (kOvl ? kChunk : 0);
     static constexpr int kBarQFull = 0;
     static constexpr int kBarKFull = 1;      // [4]
     static constexpr int kBarKEmpty = 5;     // [4]
@@ -62,14 +67,17 @@ struct DsaLayout {
     static constexpr int kBarDqFull = 13;
     static constexpr int kBarTeardown = 14;
     static constexpr int kBarDqDone = 15;    // the tile's dQ^T products have read dS^T in shared memory
-    static constexpr int kNumBars = 16;
-    static_assert(8 * kNumBars <= 8 * 16, "barrier area");
-    static constexpr int kL2eOff = kAux + 8 * 16;       // float [64]: L log2 e
+    static constexpr int kBarDkvDone = 16;   // kOvl: the tile's dKV products have read P^T / dS^T
+    static constexpr int kNumBars = 17;
+    static_assert(kNumBars <= 24, "barrier area");
+    static constexpr int kL2eOff = kAux + 8 * 24;       // float [64]: L log2 e
     static constexpr int kDOff = kL2eOff + 4 * 64;      // float [64]: D = dO . O
     static constexpr int kMiscOff = kDOff + 4 * 64;     // tmem base, abort flag
     static constexpr int kBytes = kMiscOff + 64;
     static constexpr uint32_t kTmemS = 0, kTmemDP = 64, kTmemDQ = 128, kTmemDKV = 448;
-    static_assert(kTmemDQ + 64 * kNM <= kTmemDKV, "TMEM columns");
+    // P^T and dS^T (16-bit pairs): over S^T / dP^T, or (kOvl) in the columns after dQ^T
+    static constexpr uint32_t kTmemPT = kOvl ? 384 : kTmemS, kTmemDST = kOvl ? 416 : kTmemDP;
+    static_assert(kTmemDQ + 64 * kNM <= (kOvl ? kTmemPT : kTmemDKV), "TMEM columns");
     static_assert(kBytes + 1024 <= 232448, "shared memory");
 };
 
@@ -142,6 +150,7 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         mbar_init(&bars[L::kBarDqFull], 1);
         mbar_init(&bars[L::kBarTeardown], 1);
         mbar_init(&bars[L::kBarDqDone], 1);
+        mbar_init(&bars[L::kBarDkvDone], 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -208,6 +217,11 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         for (int t = 0; t < n_tiles && ok; ++t) {
             const int key = dsa_key(p, i, len, t * kDsaTile + r);
             if (!mbar_wait(&bars[L::kBarSFull], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+            // kOvl: the previous tile's dKV products read P^T / dS^T from the columns written below
+            if (L::kOvl && t > 0 && !mbar_wait(&bars[L::kBarDkvDone], (t - 1) & 1, guard, kDevTimeoutSoftmax)) {
+                ok = false;
+                break;
+            }
             tc_fence_after();
             // Two halves of 32 heads.  P^T (16-bit pairs) goes over S^T's first 32 columns and
             // dS^T over dP^T's: half 0 writes columns 0-15 of each (heads 0-31, already in
@@ -232,8 +246,8 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     pk[e >> 1] = bf16x2_bits(p0, p1);
                     dk[e >> 1] = bf16x2_bits(g0, g1);
                 }
-                tmem_st16(tmem + lane_base + L::kTmemS + 16 * hf, pk);
-                tmem_st16(tmem + lane_base + L::kTmemDP + 16 * hf, dk);
+                tmem_st16(tmem + lane_base + L::kTmemPT + 16 * hf, pk);
+                tmem_st16(tmem + lane_base + L::kTmemDST + 16 * hf, dk);
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const uint4 v = make_uint4(dk[4 * c], dk[4 * c + 1], dk[4 * c + 2], dk[4 * c + 3]);
@@ -249,8 +263,8 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
             // its 32 rows (thread = key) around in shared memory (dS^T's buffer, free once the
             // tile's dQ^T products have read it), so that one reduction instruction covers four
             // whole 128-byte row pieces instead of 32 scattered 16-byte ones.
-            if (!mbar_wait(&bars[L::kBarDqDone], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
-            uint8_t* stage = smem + L::kDS + warp * 4096;     // 32 rows x 128 bytes
+            if (!L::kOvl && !mbar_wait(&bars[L::kBarDqDone], t & 1, guard, kDevTimeoutSoftmax)) { ok = false; break; }
+            uint8_t* stage = smem + (L::kOvl ? L::kStage : L::kDS) + warp * 4096;     // 32 rows x 128 bytes
             const int lane = r & 31;
             float* rdst[8];   // rows 4 it + lane / 8 of this warp: their accumulator rows + piece offset
 #pragma unroll
@@ -327,8 +341,27 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         bool ok = n_tiles > 0;
         if (ok && !warp_mbar_wait(&bars[L::kBarQFull], 0, guard, kDevTimeoutMma)) ok = false;
         uint32_t k = 0, j = 0;
+        // dKV chunk cc = dS^T Q[:, cc] (+ P^T dO[:, cc]), flushed by the elementwise warps
+        auto issue_dkv = [&](int cc) -> bool {
+            if (!warp_mbar_wait(&bars[L::kBarDkvFree], (j & 1) ^ 1, guard, kDevTimeoutMma)) return false;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                warp_mma_ts(tmem + L::kTmemDKV, tmem + L::kTmemDST + 8 * kk,
+                            sdesc_sw128(q_base + cc * L::kPanel + kk * 2048, L::kPanel, 1024), kIdKV, kk != 0);
+            if (cc < L::kNV) {
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    warp_mma_ts(tmem + L::kTmemDKV, tmem + L::kTmemPT + 8 * kk,
+                                sdesc_sw128(do_base + cc * L::kPanel + kk * 2048, L::kPanel, 1024), kIdKV, 1u);
+            }
+            warp_mma_commit(&bars[L::kBarDkvFull]);
+            ++j;
+            return true;
+        };
         for (int t = 0; t < n_tiles && ok; ++t) {
-            // S^T = K Q^T and dP^T = V dO^T over the key chunks
+            // S^T = K Q^T and dP^T = V dO^T over the key chunks; kOvl: the previous tile's dKV
+            // chunks kNC/2 .. kNC-1 interleaved with the first of them
             for (int c = 0; c < L::kNCE; ++c, ++k) {
                 const uint32_t slot = k & 3;
                 if (!warp_mbar_wait(&bars[L::kBarKFull + slot], (k >> 2) & 1, guard, kDevTimeoutMma)) { ok = false; break; }
@@ -346,8 +379,10 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     }
                 }
                 warp_mma_commit(&bars[L::kBarKEmpty + slot]);
+                if (L::kOvl && t > 0 && c < L::kNC / 2 && !issue_dkv(L::kNC / 2 + c)) { ok = false; break; }
             }
             if (!ok) break;
+            if (L::kOvl && t > 0) warp_mma_commit(&bars[L::kBarDkvDone]);
             warp_mma_commit(&bars[L::kBarSFull]);
             if (!warp_mbar_wait(&bars[L::kBarPReady], t & 1, guard, kDevTimeoutMma)) { ok = false; break; }
             tc_fence_after();
@@ -367,25 +402,21 @@ dsa_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                                 sdesc_sw128(ds_base + kk * 2048, L::kChunk, 1024), kIdQ, (t | kk) != 0);
                 warp_mma_commit(&bars[L::kBarKEmpty + slot]);
                 warp_mma_commit(&bars[L::kBarKEmpty + slot + 1]);
+                // kOvl: dKV chunk m of this tile between the dQ^T pairs
+                if (L::kOvl && !issue_dkv(m)) { ok = false; break; }
             }
             if (!ok) break;
             warp_mma_commit(&bars[L::kBarDqDone]);
-            // dKV chunk cc = dS^T Q[:, cc] (+ P^T dO[:, cc]), flushed by the elementwise warps
-            for (int cc = 0; cc < L::kNC; ++cc, ++j) {
-                if (!warp_mbar_wait(&bars[L::kBarDkvFree], (j & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    warp_mma_ts(tmem + L::kTmemDKV, tmem + L::kTmemDP + 8 * kk,
-                                sdesc_sw128(q_base + cc * L::kPanel + kk * 2048, L::kPanel, 1024), kIdKV, kk != 0);
-                if (cc < L::kNV) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        warp_mma_ts(tmem + L::kTmemDKV, tmem + L::kTmemS + 8 * kk,
-                                    sdesc_sw128(do_base + cc * L::kPanel + kk * 2048, L::kPanel, 1024), kIdKV, 1u);
-                }
-                warp_mma_commit(&bars[L::kBarDkvFull]);
+            if (!L::kOvl) {
+                for (int cc = 0; cc < L::kNC && ok; ++cc)
+                    if (!issue_dkv(cc)) ok = false;
             }
+        }
+        if (L::kOvl && ok && n_tiles > 0) {
+            // the last tile's remaining dKV chunks
+            for (int cc = L::kNC / 2; cc < L::kNC && ok; ++cc)
+                if (!issue_dkv(cc)) ok = false;
+            if (ok) warp_mma_commit(&bars[L::kBarDkvDone]);
         }
         if (ok && n_tiles > 0) warp_mma_commit(&bars[L::kBarDqFull]);
         warp_mma_commit(&bars[L::kBarTeardown]);
