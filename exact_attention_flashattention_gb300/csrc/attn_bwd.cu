@@ -35,11 +35,13 @@ namespace {
 constexpr int kThreads = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kPanelBytes = 128 * 128;
-// SM cycles over which a d = 128 dQ drain spreads one tile's accumulator reductions: about
-// two thirds of a tile's period on this GPU.  Measured on the causal B=8 H=16 N=4096 d=128
-// backward: 1500 -> 4000 cycles gave 1.28, 1.28, 1.26, 1.23, 1.29, 1.30 ms against 1.38 ms
-// unpaced (the window also bounds how late the drain can start the next tile).
-constexpr long long kDqPaceCycles = 3000;
+// SM cycles over which a dQ drain spreads one tile's accumulator reductions (the window also
+// bounds how late the drain can start the next tile).  Measured, backward of causal B=8 H=16
+// N=4096 d=128: 1500 / 2000 / 2500 / 2750 / 3000 / 3250 / 3500 / 4000 cycles gave 1.28 / 1.28 /
+// 1.26 / 1.23 / 1.22 / 1.24 / 1.29 / 1.30 ms against 1.38 ms unpaced; causal B=4 H=16 N=4096
+// d=64: 1500 / 2500 / 3000 / 3500 gave 0.586 / 0.562 / 0.518 / 0.516 ms against 0.592.
+template <int D>
+constexpr long long kDqPaceCycles = D == 128 ? 3000 : 3500;
 
 // ---------------------------------------------------------------- preprocess
 // ndelta_r = -scale * sum_c dO[r,c] O[r,c] (FP32: the negated D of the
@@ -431,7 +433,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 128; ++e) {
                             red_add_f32(dst + (size_t)e * D, __uint_as_float(r[e]));
                             if ((e & 3) == 3 && e < 127) {
-                                const long long due = t0 + (long long)(e + 1) * kDqPaceCycles / 128;
+                                const long long due = t0 + (long long)(e + 1) * kDqPaceCycles<D> / 128;
                                 while (clock64() < due) {}
                             }
                         }
@@ -444,10 +446,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         tmem_wait_ld();
                         tc_fence_before();
                         mbar_arrive(&bars[L::kBarDqFree]);
+                        // paced as at d = 128: one 16-byte reduction every kDqPaceCycles / 16 cycles
+                        const long long t0 = clock64();
 #pragma unroll
-                        for (int e = 0; e < 16; ++e)
+                        for (int e = 0; e < 16; ++e) {
                             red_add_v4(dst + 4 * e, __uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
                                        __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
+                            if (e < 15) {
+                                const long long due = t0 + (long long)(e + 1) * kDqPaceCycles<D> / 16;
+                                while (clock64() < due) {}
+                            }
+                        }
                     }
                 }
                 if (!ok) break;
