@@ -401,6 +401,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         uint32_t g = 0;
         int k = 0;
         bool ok = true;
+        const bool kv_al32 = ((reinterpret_cast<uintptr_t>(dk_out) | reinterpret_cast<uintptr_t>(dv_out)) & 31u) == 0;
         BwdUnits<kDyn> units(n_units);
         for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutCorr)) >= 0;) {
             for (int sidx = 0; sidx < 2 && ok; ++sidx, ++k) {
@@ -478,10 +479,17 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         for (int e = 0; e < 16; ++e)
                             pk[e] = pack2<BF16>(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
                         if (row_valid) {
-                            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
+                            // one row per thread: 32-byte stores fill whole sectors (rows start at
+                            // multiples of 128 bytes, so a 32-byte aligned base suffices)
+                            if (kv_al32) {
+                                st_global_v8(dst + c * 2, &pk[0]);
+                                st_global_v8(dst + c * 2 + 32, &pk[8]);
+                            } else {
+                                uint4* d4 = reinterpret_cast<uint4*>(dst + c * 2);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e)
-                                d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                                for (int e = 0; e < 4; ++e)
+                                    d4[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                            }
                         }
                     }
                 }
