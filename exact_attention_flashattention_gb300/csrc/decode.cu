@@ -14,10 +14,11 @@
 //    (b, hkv) are the rows of one zero-padded 128-row Q tile, so one
 //    S = Q K^T MMA (tcgen05, M = 128) serves all of them and K / V are read
 //    once per group;
-//  * split KV: the keys of a group are cut into chunks of 512 KB of K / V
-//    (1024 keys at d = 128, 2048 at d = 64), and a
-//    persistent grid (one CTA per SM) walks the (group, chunk) items, so that
-//    even a small batch covers every SM with little tail; each item writes its
+//  * split KV: the keys of a group are cut into chunks of whole 128-key tiles,
+//    at least 512 KB of K / V (1024 keys at d = 128, 2048 at d = 64), their
+//    length chosen per launch so that the (group, chunk) items fill the
+//    persistent grid (one CTA per SM) in whole waves, so that even a small
+//    batch covers every SM with little tail; each item writes its
 //    chunk's O (normalised) and L, and a second kernel combines the chunks:
 //    L = log sum_s exp(L_s), O = sum_s exp(L_s - L) O_s;
 //  * per chunk the pipeline of the forward kernel, reduced to one Q tile: a
