@@ -114,8 +114,8 @@ def test_decode_argument_checks_before_any_launch(lib):
     null = vp(0)
     d = lib.attn_decode
     wsz = attn.attn_decode_workspace_size
-    # chunks of 1024 keys at d = 128 (2048 at d = 64); per (group, chunk, query head): d FP32
-    # values and one L
+    # sized for the finest split, chunks of 1024 keys at d = 128 (2048 at d = 64; a launch may use
+    # longer ones); per (group, chunk, query head): d FP32 values and one L
     rows = 2 * 2 * 3 * 4                    # B Hkv, 3 chunks of 3000 keys, G = 4
     up = lambda x: (x + 255) // 256 * 256
     assert wsz(2, 8, 2, 3000, 128) == up(up(rows * 128 * 4) + rows * 4)
