@@ -11,16 +11,24 @@ value        whole-job TFLOPS of the step, FLOP convention fwd 4 B H N^2 d and
              bwd 10 B H N^2 d, each halved for causal; inputs resident in HBM.
 e2e          the same metric through the C ABI with HOST (pinned) buffers:
              q, k, v, dO copied in and o, lse, dq, dk, dv copied out every step.
+fwd_pct_peak / bwd_pct_peak
+             % of the GB300 dense BF16 tensor peak at the SM clock sampled
+             during the timed region (SMs x 8192 FLOP/clk x MHz); the same
+             against the measured cuBLAS burst and sustained peaks alongside.
 roofline     the backward main kernel (the dominant one): its algorithmic FLOPs
-             per launch / its CUDA-event duration, against the measured
-             sustained bf16 peak; traffic from a committed ncu capture when it
-             matches the current kernel source, else null.
+             per launch / its median CUDA-event duration, against the measured
+             burst bf16 peak (the kernel is timed launch by launch); traffic
+             from a committed ncu capture when it matches the current kernel
+             source, else null.
 cpu_baseline the FP64 oracle, as it stands, on a bounded sample of the same
              workload on this host's cores (rank 0, N=1 only).
 --impl reference  times that oracle alone, each step a bounded sample.
 
-Multi-GPU (torchrun): every rank runs its own copy of the workload (heads are
-independent, no data-path collective); value = all ranks' FLOPs / max time.
+Multi-GPU: every rank runs its own copy of the workload on its own GPU (heads
+are independent, no data-path collective); value = all ranks' FLOPs / max time.
+Launched under torchrun (RANK / WORLD_SIZE set) each process is one rank; with
+--gpus N > 1 and no WORLD_SIZE, bench.py starts the N ranks itself through
+torch.distributed.run (rendezvous on 127.0.0.1).
 """
 from __future__ import annotations
 
@@ -53,6 +61,15 @@ def load_peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+# Dense BF16 tensor-core work per SM per clock on sm_103a: one 128 x 256 x 16 MMA (2 x 128 x 256 x 16
+# FLOP) every 128 cycles.
+NOMINAL_FLOP_PER_CLK = 8192
+
+
+def nominal_bf16_tflops(n_sm, sm_mhz):
+    return n_sm * NOMINAL_FLOP_PER_CLK * sm_mhz * 1e6 / 1e12
 
 
 # The sources the attention forward / backward kernels are compiled from (the other kernels of
@@ -303,11 +320,11 @@ def run_ours(args):
         raise RuntimeError("device error word set during the timed region")
 
     total_ms = t_start.elapsed_time(t_end)
-    fwd_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
-    pre_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
-    main_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    conv_ms = statistics.mean(e[3].elapsed_time(e[4]) for e in evs)
-    fwd_med = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    fwd_ms = statistics.median(e[0].elapsed_time(e[1]) for e in evs)
+    pre_ms = statistics.median(e[1].elapsed_time(e[2]) for e in evs)
+    main_ms = statistics.median(e[2].elapsed_time(e[3]) for e in evs)
+    conv_ms = statistics.median(e[3].elapsed_time(e[4]) for e in evs)
+    fwd_med = fwd_ms
     bwd_med = statistics.median(e[1].elapsed_time(e[4]) for e in evs)
     ms_per_step = max_over_ranks(total_ms / args.steps, world)
     value = (fwd_fl + bwd_fl) * world / ms_per_step / 1e9
@@ -387,7 +404,10 @@ def run_ours(args):
     traffic = committed_traffic("attn_bwd_kernel<128,bf16>")
     fwd_tf = fwd_fl / fwd_med / 1e9
     bwd_tf = bwd_fl / bwd_med / 1e9
-
+    # The tensor pipe's dense rate at the SM clock sampled during the timed region (the clock the
+    # kernels ran at), or at the maximum clock when no sample could be taken.
+    sm_mhz = clocks["sm_mhz"] if clocks else float(peaks.get("sm_max_mhz", 2070.0))
+    nominal = nominal_bf16_tflops(n_sm, sm_mhz)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         n_heads = min(host_cores(), 16)
@@ -415,25 +435,28 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (q, k, v, dO: 134 MB each; 129 MB L2), no flush"},
         "fwd_tflops": fwd_tf,
         "bwd_tflops": bwd_tf,
-        "fwd_pct_peak": 100.0 * fwd_tf / peak_burst,
-        "bwd_pct_peak": 100.0 * bwd_tf / peak_burst,
-        "pct_peak_basis": f"bf16_tflops (burst) = {peak_burst} TFLOP/s, {peak_src}",
-        "fwd_pct_sustained_peak": 100.0 * fwd_tf / peak_sus,
-        "bwd_pct_sustained_peak": 100.0 * bwd_tf / peak_sus,
-        "nominal_peak_at_clock": (None if not clocks else {
-            "tflops": n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12, "sms": n_sm, "sm_mhz": clocks["sm_mhz"],
-            "basis": "SMs x 8192 dense bf16 FLOP/clk/SM (one 128x256x16 MMA per 128 cycles) x median SM clock",
-            "fwd_pct": 100.0 * fwd_tf / (n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12),
-            "bwd_pct": 100.0 * bwd_tf / (n_sm * 8192 * clocks["sm_mhz"] * 1e6 / 1e12)}),
-        "kernel_ms": {"attn_fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms, "bwd_dq_convert": conv_ms},
+        "fwd_pct_peak": 100.0 * fwd_tf / nominal,
+        "bwd_pct_peak": 100.0 * bwd_tf / nominal,
+        "pct_peak_basis": (f"GB300 dense BF16 tensor peak at the SM clock: {n_sm} SMs x {NOMINAL_FLOP_PER_CLK} "
+                           f"FLOP/clk/SM x {sm_mhz:.0f} MHz ({'median sampled during the timed region' if clocks else 'maximum clock, no sample'}) "
+                           f"= {nominal:.1f} TFLOP/s"),
+        "fwd_pct_measured_burst_peak": 100.0 * fwd_tf / peak_burst,
+        "bwd_pct_measured_burst_peak": 100.0 * bwd_tf / peak_burst,
+        "fwd_pct_measured_sustained_peak": 100.0 * fwd_tf / peak_sus,
+        "bwd_pct_measured_sustained_peak": 100.0 * bwd_tf / peak_sus,
+        "measured_peaks": {"bf16_tflops": peak_burst, "bf16_tflops_sustained": peak_sus, "source": peak_src},
+        "kernel_ms": {"attn_fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms, "bwd_dq_convert": conv_ms,
+                      "statistic": f"median over the {args.steps} timed steps (CUDA events per kernel)"},
         "roofline": {
             "kernel": "attn_bwd_kernel<128,bf16> (backward main)",
             "bound": "tensor",
             "achieved": main_tflops,
-            "peak": peak_sus,
+            "peak": peak_burst,
             "unit": "TFLOP/s",
-            "frac": main_tflops / peak_sus,
-            "peak_kind": f"bf16_tflops_sustained, {peak_src}",
+            "frac": main_tflops / peak_burst,
+            "peak_kind": f"bf16_tflops (cuBLAS burst; the kernel is timed launch by launch), {peak_src}",
+            "sm_mhz": sm_mhz,
+            "frac_of_nominal_at_clock": main_tflops / nominal,
             "traffic": traffic,
             "algorithmic_flops_per_launch": bwd_fl,
         },
@@ -444,6 +467,22 @@ def run_ours(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def time_calls(fn, stream, iters, warmup):
+    """Median device time of one call of fn (ms): `warmup` untimed calls, then `iters` calls
+    each bracketed by CUDA events on `stream`."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(iters)]
+    torch.cuda.synchronize()
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
 
 
 SWEEP = [
@@ -483,33 +522,17 @@ DSA_SWEEP = [
 
 
 def dsa_prepare(s_q, s_kv, H, d_qk, topk, causal, seed=17):
-    """Synthetic inputs of the sparse top-k backward on the GPU: q, kv, dO ~ N(0, 1) bf16,
-    sink ~ N(0, 1), each row's list = topk distinct random keys (keys 0..i when causal,
-    padded with -1), and the forward's O (bf16) and L (FP32) from a plain PyTorch FP32
-    computation over the gathered keys (input preparation, not timed)."""
+    """Synthetic inputs of the sparse top-k backward on the GPU (seeded_inputs.dsa_device_draws:
+    q, kv, dO ~ N(0, 1) bf16, sink ~ N(0, 1), each row's list = topk distinct random keys,
+    keys 0..i when causal, padded with -1) and the forward's O (bf16) and L (FP32) from a
+    plain PyTorch FP32 computation over the gathered keys (input preparation, not timed)."""
     import torch
+
+    import seeded_inputs as si
     dev = torch.device("cuda", 0)
-    g = torch.Generator(device=dev)
-    g.manual_seed(seed)
     d_v = 512
-    q = torch.randn((s_q, H, d_qk), generator=g, device=dev).to(torch.bfloat16)
-    kv = torch.randn((s_kv, d_qk), generator=g, device=dev).to(torch.bfloat16)
-    do = torch.randn((s_q, H, d_v), generator=g, device=dev).to(torch.bfloat16)
-    sink = torch.randn((H,), generator=g, device=dev)
-    idx = torch.empty((s_q, topk), dtype=torch.int32, device=dev)
-    lens = torch.empty((s_q,), dtype=torch.int32, device=dev)
-    for r0 in range(0, s_q, 512):
-        r1 = min(s_q, r0 + 512)
-        keys = torch.rand((r1 - r0, s_kv), generator=g, device=dev)
-        rows = torch.arange(r0, r1, device=dev)[:, None]
-        if causal:
-            keys = torch.where(torch.arange(s_kv, device=dev)[None, :] <= rows, keys, torch.full_like(keys, 2.0))
-        order = keys.argsort(dim=1)[:, :topk].to(torch.int32)
-        n = torch.clamp(rows[:, 0] + 1, max=min(topk, s_kv)) if causal else torch.full((r1 - r0,), min(topk, s_kv),
-                                                                                     device=dev)
-        pos = torch.arange(topk, device=dev)[None, :]
-        idx[r0:r1] = torch.where(pos < n[:, None], order, torch.full_like(order, -1))
-        lens[r0:r1] = n.to(torch.int32)
+    x = si.dsa_device_draws(s_q, s_kv, H, d_qk, topk, causal, seed=seed, d_v=d_v)
+    q, kv, sink, idx = x["q"], x["kv"], x["sink"], x["idx"]
     o = torch.empty((s_q, H, d_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((s_q, H), dtype=torch.float32, device=dev)
     scale = d_qk ** -0.5
@@ -526,7 +549,7 @@ def dsa_prepare(s_q, s_kv, H, d_qk, topk, causal, seed=17):
         P = torch.exp(S - L[:, :, None])
         o[r0:r1] = torch.einsum("rhk,rkd->rhd", P, K[:, :, :d_v]).to(torch.bfloat16)
         lse[r0:r1] = L
-    return dict(q=q, kv=kv, do=do, sink=sink, idx=idx, lens=lens, o=o, lse=lse, scale=scale)
+    return dict(x, o=o, lse=lse, scale=scale)
 
 
 def dsa_flops(s_q, H, d_qk, topk, d_v=512, entries=None):
@@ -537,9 +560,10 @@ def dsa_flops(s_q, H, d_qk, topk, d_v=512, entries=None):
     return 2.0 * n * H * (3 * d_qk + 2 * d_v)
 
 
-def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=True):
-    """Time attn_dsa_bwd (its memsets and both kernels) with CUDA events; one JSON line with
-    TFLOPS by dsa_flops and the fraction of the measured dense BF16 peak."""
+def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=100, warmup=20, build=True):
+    """Time attn_dsa_bwd (its memsets and both kernels) with CUDA events (median of `iters`
+    calls); one JSON line with TFLOPS by dsa_flops and the fraction of the measured dense
+    BF16 peak."""
     import torch
 
     if build:
@@ -560,16 +584,7 @@ def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=Tr
         attn.attn_dsa_bwd(x["q"], x["kv"], x["o"], x["do"], x["lse"], x["sink"], x["idx"], x["lens"], dq, dkv, dsink,
                           ws, x["scale"], causal, stream)
 
-    for _ in range(warmup):
-        call()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    a.record(stream)
-    for _ in range(iters):
-        call()
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / iters
+    ms = time_calls(call, stream, iters, warmup)
     if attn.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error word set")
     tf = dsa_flops(s_q, H, d_qk, topk, entries=int(x["lens"].sum().item())) / ms / 1e9
@@ -579,9 +594,9 @@ def run_dsa(s_q, s_kv, H, d_qk, topk, causal=False, iters=20, warmup=3, build=Tr
     return 0
 
 
-def run_sweep(iters=20):
-    """Forward and backward TFLOPS of every workload of the list (CUDA events,
-    3 warm-up calls, `iters` timed calls each).  One JSON line per workload;
+def run_sweep(iters=100, warmup=20):
+    """Forward and backward TFLOPS of every workload of the list (CUDA events around each
+    call, `warmup` untimed and `iters` timed calls, median).  One JSON line per workload;
     not the bench contract line."""
     import torch
 
@@ -605,16 +620,7 @@ def run_sweep(iters=20):
         sc = d ** -0.5
 
         def timed(fn):
-            for _ in range(3):
-                fn()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            a.record(stream)
-            for _ in range(iters):
-                fn()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            return a.elapsed_time(b) / iters
+            return time_calls(fn, stream, iters, warmup)
 
         fms = timed(lambda: attn.attn_fwd(q, k, v, o, lse, sc, causal, stream))
         bms = timed(lambda: attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, sc, causal, stream))
@@ -654,16 +660,7 @@ def run_sweep(iters=20):
         sc = d ** -0.5
 
         def timed_l(fn):
-            for _ in range(3):
-                fn()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize(dev)
-            a.record(stream)
-            for _ in range(iters):
-                fn()
-            b.record(stream)
-            torch.cuda.synchronize(dev)
-            return a.elapsed_time(b) / iters
+            return time_calls(fn, stream, iters, warmup)
 
         fms = timed_l(lambda: attn.attn_fwd_layout(q, k, v, o, lse, sc, True, layout, cu, maxlen, stream))
         bms = timed_l(lambda: attn.attn_bwd_layout(q, k, v, o, do, lse, dq, dk, dv, ws, sc, True, layout, cu, maxlen,
@@ -674,15 +671,16 @@ def run_sweep(iters=20):
                           "bwd_ms": bms, "bwd_tflops": flop_b / bms / 1e9}), flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
     for name, B, Hq, Hkv, N, d in DECODE_SWEEP:
-        run_decode(name, B, Hq, Hkv, N, d, iters=iters, warmup=3, build=False)
+        run_decode(name, B, Hq, Hkv, N, d, iters=iters, warmup=warmup, build=False)
     for s, H, d_qk, topk in DSA_SWEEP:
-        run_dsa(s, s, H, d_qk, topk, iters=iters, warmup=3, build=False)
+        run_dsa(s, s, H, d_qk, topk, iters=iters, warmup=warmup, build=False)
     return 0
 
 
-def run_decode(name, B, Hq, Hkv, N, d, iters=20, warmup=3, build=True):
+def run_decode(name, B, Hq, Hkv, N, d, iters=100, warmup=20, build=True):
     """Decode against a key/value cache: HBM-bound, reported in GB/s of the cache bytes read
-    (CUDA events, `warmup` untimed and `iters` timed calls of attn_decode).  One JSON line."""
+    (CUDA events, `warmup` untimed and `iters` timed calls of attn_decode, median).  One JSON
+    line."""
     import torch
 
     if build:
@@ -699,16 +697,8 @@ def run_decode(name, B, Hq, Hkv, N, d, iters=20, warmup=3, build=True):
     kc, vc = (torch.randn((B, Hkv, N, d), generator=g, device=dev).to(torch.bfloat16) for _ in range(2))
     o, lse = torch.empty_like(q), torch.empty((B, Hq), device=dev)
     ws = torch.empty(attn.attn_decode_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
-    for _ in range(warmup):
-        attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    a.record(stream)
-    for _ in range(iters):
-        attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream)
-    b.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = a.elapsed_time(b) / iters
+    ms = time_calls(lambda: attn.attn_decode(q, kc, vc, o, lse, ws, d ** -0.5, None, stream), stream, iters,
+                    warmup)
     if attn.attn_last_device_error(stream) != 0:
         raise RuntimeError("device error word set")
     cache_bytes = 2 * B * Hkv * N * d * 2          # K and V, each read once
@@ -717,6 +707,18 @@ def run_decode(name, B, Hq, Hkv, N, d, iters=20, warmup=3, build=True):
                       "gbs": gbs, "pct_hbm": 100 * gbs / hbm, "peak_basis": f"HBM copy {hbm} GB/s ({src})"}),
           flush=True)
     return 0
+
+
+def spawn_ranks(n, argv):
+    """Start n ranks of this script with torch.distributed.run on this node (one per GPU,
+    LOCAL_RANK = GPU index) and return the launcher's exit code.  Rank 0 prints the line."""
+    import socket
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.abspath(__file__)] + list(argv)
+    return subprocess.call(cmd)
 
 
 def main():
@@ -745,6 +747,8 @@ def main():
                          .format("causal" if WORKLOAD["causal"] else "non-causal", **WORKLOAD))
     if args.warmup < 3:
         args.warmup = 3
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not (args.sweep or args.decode_shape or args.dsa_shape):
+        return spawn_ranks(args.gpus, sys.argv[1:])
     if args.sweep:
         return run_sweep()
     if args.decode_shape:

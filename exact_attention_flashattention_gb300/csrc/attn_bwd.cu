@@ -91,7 +91,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ 
                 acc = fmaf(fa.y, fb.y, acc);
             }
         }
-        const unsigned mask = __activemask();
+        // The TPR lanes of a row (an aligned group: blocks are whole warps and total is a multiple
+        // of TPR) take every branch together, so the shuffle names exactly that group.
+        const unsigned lane = threadIdx.x & 31u;
+        const unsigned mask = (TPR >= 32) ? 0xffffffffu : (((1u << TPR) - 1u) << (lane & ~(unsigned)(TPR - 1)));
 #pragma unroll
         for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
         dq_acc[2 * (wrow * TPR + part)] = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -5,10 +5,12 @@
 // inputs and outputs), or run where cudaMalloc's implicit synchronisation or
 // its out-of-memory failure mid-run is not acceptable.  attn_bwd needs a
 // caller-provided workspace; this entry point instead uses scratch memory that
-// is part of the library image itself: the file-scope device array below,
-// which the CUDA driver reserves on each GPU when it loads this library's
-// device code and keeps until the process exits.  It calls no cudaMalloc,
-// cudaFree or other allocating routine.
+// is part of the library image itself: the file-scope device array below.
+// The CUDA driver reserves it on a GPU when it loads this file's device code
+// (under the default lazy module loading, at the first call's address lookup
+// on that GPU; at library load with CUDA_MODULE_LOADING=EAGER) and keeps it
+// until the process exits.  It calls no cudaMalloc, cudaFree or other
+// allocating routine.
 #include <mutex>
 
 #include "../../include/attn.h"

@@ -188,9 +188,14 @@ ATTN_API attn_status_t attn_bwd_stage(int stage, const void *q, const void *k, c
  * Same computation and arguments as attn_bwd_ex, minus the workspace: the
  * scratch it needs (attn_bwd_workspace_size(B, H, N, d) bytes) comes from one
  * fixed device array of ATTN_NOALLOC_SCRATCH_BYTES inside this library.  The
- * driver reserves that array on each GPU when it loads the library's device
- * code, and it stays reserved until the process exits.  No call allocates or
- * frees memory.
+ * driver reserves that array on a GPU when it loads the device code that holds
+ * it: under CUDA's default lazy module loading that is the first
+ * attn_bwd_noalloc call on that GPU (which resolves the array's address), and
+ * the library load itself only with CUDA_MODULE_LOADING=EAGER.  That first
+ * call can therefore fail with ATTN_ERR_CUDA if the GPU has less than
+ * ATTN_NOALLOC_SCRATCH_BYTES free; a caller that needs the reservation up
+ * front makes one call at start-up.  The array then stays reserved until the
+ * process exits, and no call allocates or frees memory.
  *  - Sizes whose scratch exceeds ATTN_NOALLOC_SCRATCH_BYTES return
  *    ATTN_ERR_WORKSPACE and queue nothing; other argument errors are those of
  *    attn_bwd_ex.

@@ -196,3 +196,38 @@ def dsa_inputs(base_seed: int, s_q: int, s_kv: int, H: int, d_qk: int, d_v: int,
     out["sink"] = standard_normal(head_key(base_seed, TENSOR_IDS["sink"], 0), H)
     out["idx"], out["lens"] = topk_indices(base_seed, s_q, s_kv, topk, causal, rows)
     return out
+
+
+def dsa_device_draws(s_q: int, s_kv: int, H: int, d_qk: int, topk: int, causal: bool, seed: int = 17,
+                     d_v: int = 512, device: str = "cuda") -> dict:
+    """Sparse top-k attention inputs drawn on the GPU with torch's generator, for sizes where
+    the host generator above is too slow (full-size timing and sampled checks): q [s_q, H,
+    d_qk], kv [s_kv, d_qk], do [s_q, H, d_v] ~ N(0, 1) rounded to bf16; sink [H] ~ N(0, 1)
+    float32; each row's list = min(topk, n_i) distinct random keys (keys 0..i when causal,
+    n_i = i + 1, else s_kv), padded with -1; lens [s_q] the list lengths.  Draws only: the
+    forward's O and L, which the backward also takes, are for the caller to compute."""
+    import torch
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    q = torch.randn((s_q, H, d_qk), generator=g, device=dev).to(torch.bfloat16)
+    kv = torch.randn((s_kv, d_qk), generator=g, device=dev).to(torch.bfloat16)
+    do = torch.randn((s_q, H, d_v), generator=g, device=dev).to(torch.bfloat16)
+    sink = torch.randn((H,), generator=g, device=dev)
+    idx = torch.empty((s_q, topk), dtype=torch.int32, device=dev)
+    lens = torch.empty((s_q,), dtype=torch.int32, device=dev)
+    for r0 in range(0, s_q, 512):
+        r1 = min(s_q, r0 + 512)
+        keys = torch.rand((r1 - r0, s_kv), generator=g, device=dev)
+        rows = torch.arange(r0, r1, device=dev)[:, None]
+        if causal:
+            keys = torch.where(torch.arange(s_kv, device=dev)[None, :] <= rows, keys, torch.full_like(keys, 2.0))
+        order = keys.argsort(dim=1)[:, :topk].to(torch.int32)
+        if causal:
+            n = torch.clamp(rows[:, 0] + 1, max=min(topk, s_kv))
+        else:
+            n = torch.full((r1 - r0,), min(topk, s_kv), device=dev)
+        pos = torch.arange(topk, device=dev)[None, :]
+        idx[r0:r1] = torch.where(pos < n[:, None], order, torch.full_like(order, -1))
+        lens[r0:r1] = n.to(torch.int32)
+    return dict(q=q, kv=kv, do=do, sink=sink, idx=idx, lens=lens)

@@ -138,16 +138,37 @@ def _sub_bwd(x, rows, idx_rows, scale, causal):
                           t(x["sink"]), idx_rows, None, scale, causal, 512)
 
 
+def _forward_inputs(x, scale, d_v=512):
+    """The backward's O (bf16) and L (FP32) inputs at full size, from a plain PyTorch FP32
+    forward over each row's gathered keys with the sink in the denominator (input
+    preparation: the oracle's backward is given these same O and L)."""
+    q, kv, sink, idx = x["q"], x["kv"], x["sink"], x["idx"]
+    s_q, H = q.shape[0], q.shape[1]
+    o = torch.empty((s_q, H, d_v), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((s_q, H), dtype=torch.float32, device="cuda")
+    kvf = kv.float()
+    for r0 in range(0, s_q, 64):
+        r1 = min(s_q, r0 + 64)
+        ix = idx[r0:r1].long()
+        K = kvf[ix.clamp(min=0)]
+        S = torch.einsum("rhd,rkd->rhk", q[r0:r1].float(), K) * scale
+        S = S.masked_fill(~(ix >= 0)[:, None, :], float("-inf"))
+        L = torch.logsumexp(torch.cat([S, sink[None, :, None].expand(r1 - r0, H, 1)], dim=2), dim=2)
+        o[r0:r1] = torch.einsum("rhk,rkd->rhd", torch.exp(S - L[:, :, None]), K[:, :, :d_v]).to(torch.bfloat16)
+        lse[r0:r1] = L
+    return o, lse
+
+
 def test_dsa_bwd_full_size_sampled(attn):
     """s_q = s_kv = 4096, H = 128, QK 576, top-k 2048 (the largest shape of the pull
     request's table), sink on, launched as bench.py times it.  dQ on sampled queries;
     dKV on sampled keys (L is an input, so each listed (query, key) entry contributes on
     its own: the oracle runs on the queries that list the key, each with that one entry);
     dSink over all rows, 256 at a time."""
-    from bench import dsa_prepare
     s, H, d_qk, topk = 4096, 128, 576, 2048
-    x = dsa_prepare(s, s, H, d_qk, topk, False)
-    scale = x["scale"]
+    x = si.dsa_device_draws(s, s, H, d_qk, topk, False, seed=17)
+    scale = d_qk ** -0.5
+    x["o"], x["lse"] = _forward_inputs(x, scale)
     dq = torch.full_like(x["q"], float("nan"))
     dkv = torch.full_like(x["kv"], float("nan"))
     dsink = torch.full_like(x["sink"], float("nan"))

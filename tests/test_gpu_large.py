@@ -1,16 +1,16 @@
 """CUDA path vs the FP64 oracle at the full sizes of the workload list, in the
 launch configuration bench.py times (persistent grid over every head).
 
-Whole heads are too slow for the oracle at these sizes, so it checks outputs it
-can compute one by one:
-  * O, L and dQ of sampled query rows (first and last rows, tile edges, random
-    rows) of sampled heads -- each needs one row of S, P, dP, dS;
-  * dK and dV of the last key tile under the causal mask, which only the last
-    128 query rows reach, so the oracle's sum over those rows is complete;
-  * for non-causal heads, dK and dV of one whole head (oracle rows split over
-    threads and summed);
+Per configuration:
+  * whole heads: dQ, dK and dV of every row of at least two heads (head 0 and
+    the last head; two more seeded heads where N <= 8192) from the oracle's
+    row-set entry point, the rows split over threads and the dK / dV
+    contributions summed; O and L of every row of head 0 and of the last head;
+  * sampled query rows (first and last rows, tile edges, random rows) of those
+    heads and two more: O, L and dQ, each needing one row of S, P, dP, dS;
 and, on every head, properties that hold at any size: no NaN / unwritten
 element, and sum_j dK_j = 0 (rows of dS sum to zero).
+The worst error of each quantity over the checked heads is printed.
 """
 import math
 import os
@@ -62,18 +62,31 @@ def _sample_rows(N, rng):
     return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
 
 
-def _whole_head_dkdv(q, k, v, do, scale, causal, threads):
-    """dK, dV of one head from the oracle's row-set entry point, rows split over threads."""
+def _whole_head_bwd(q, k, v, do, scale, causal, threads):
+    """dQ, dK, dV of every row of one head from the oracle's row-set entry point.  Rows are
+    dealt round robin to the threads (so causal rows of different cost spread evenly); each
+    thread returns its rows' dQ and their contributions to dK and dV, which are summed."""
     N = q.shape[0]
-    chunks = np.array_split(np.arange(N, dtype=np.int64), threads)
+    chunks = [np.arange(t, N, threads, dtype=np.int64) for t in range(min(threads, N))]
 
     def one(rows):
-        _, dk, dv = oracle.attn_bwd_rowset(q, k, v, do, rows, scale, causal)
-        return dk, dv
+        return oracle.attn_bwd_rowset(q, k, v, do, rows, scale, causal)
 
-    with ThreadPoolExecutor(threads) as ex:
+    with ThreadPoolExecutor(len(chunks)) as ex:
         parts = list(ex.map(one, chunks))
-    return sum(p[0] for p in parts), sum(p[1] for p in parts)
+    dq = np.empty_like(q)
+    for rows, p in zip(chunks, parts):
+        dq[rows] = p[0]
+    return dq, sum(p[1] for p in parts), sum(p[2] for p in parts)
+
+
+def _whole_heads(BH, N):
+    """Heads checked whole: head 0 and the last head, plus two seeded ones when N <= 8192."""
+    heads = {0, BH - 1}
+    if N <= 8192:
+        rng = np.random.default_rng(7 * BH + N)
+        heads.update(int(x) for x in rng.choice(BH, size=min(2, BH), replace=False))
+    return sorted(heads)
 
 
 @pytest.mark.parametrize("cid,B,H,N,d,causal,dtype,sigma", CONFIGS, ids=[c[0] for c in CONFIGS])
@@ -101,11 +114,17 @@ def test_full_size_against_oracle(attn, cid, B, H, N, d, causal, dtype, sigma):
     colabs = dkf.abs().sum(dim=2) + 1e-6
     assert float((colsum / colabs).max()) < 2e-2, "sum_j dK_j != 0"
 
+    og, lg = to_f64(o).reshape(BH, N, d), to_f64(lse).reshape(BH, N)
+    dqg, dkg, dvg = (to_f64(t).reshape(BH, N, d) for t in (dq, dk, dv))
+    del o, lse, dq, dk, dv, ws
+    x_of = lambda h: {n: si.bits_to_f32(bits[n][h], dtype).astype(np.float64) for n in bits}
+    worst = {n: 0.0 for n in ("o", "l", "dq_rows", "dq", "dk", "dv")}
+    per_head = []
+
+    # sampled rows: O, L, dQ
     rng = np.random.default_rng(N + d)
-    worst = {"o": 0.0, "l": 0.0, "dq": 0.0, "dkdv_tail": 0.0}
-    og, lg, dqg = to_f64(o).reshape(BH, N, d), to_f64(lse).reshape(BH, N), to_f64(dq).reshape(BH, N, d)
     for h in _sample_heads(BH):
-        x = {n: si.bits_to_f32(bits[n][h], dtype).astype(np.float64) for n in bits}
+        x = x_of(h)
         rows = _sample_rows(N, rng)
         o_r, l_r, dq_r = oracle.attn_rows(x["q"], x["k"], x["v"], rows, scale, causal, dout=x["do"])
         err = np.abs(og[h][rows] - o_r)
@@ -116,26 +135,30 @@ def test_full_size_against_oracle(attn, cid, B, H, N, d, causal, dtype, sigma):
         worst["l"] = max(worst["l"], le)
         e = rel_fro(dqg[h][rows], dq_r)
         assert e <= TOL_GRAD_RELFRO, (h, "dq rows", e)
-        worst["dq"] = max(worst["dq"], e)
-    # dK, dV checked exactly where the oracle can afford them
-    dkg, dvg = to_f64(dk).reshape(BH, N, d), to_f64(dv).reshape(BH, N, d)
-    h = BH - 1
-    x = {n: si.bits_to_f32(bits[n][h], dtype).astype(np.float64) for n in bits}
-    if causal:
-        tail = np.arange(N - 128, N, dtype=np.int64)
-        dq_t, dk_t, dv_t = oracle.attn_bwd_rowset(x["q"], x["k"], x["v"], x["do"], tail, scale, causal)
-        for name, got, ref in (("dq", dqg[h][tail], dq_t), ("dk", dkg[h][tail], dk_t[tail]),
-                               ("dv", dvg[h][tail], dv_t[tail])):
-            e = rel_fro(got, ref)
-            assert e <= TOL_GRAD_RELFRO, (name, "last tile", e)
-            worst["dkdv_tail"] = max(worst["dkdv_tail"], e)
-    elif N <= 8192:
-        dk_r, dv_r = _whole_head_dkdv(x["q"], x["k"], x["v"], x["do"], scale, causal, threads)
-        for name, got, ref in (("dk", dkg[h], dk_r), ("dv", dvg[h], dv_r)):
-            e = rel_fro(got, ref)
-            assert e <= TOL_GRAD_RELFRO, (name, "whole head", e)
-            worst["dkdv_tail"] = max(worst["dkdv_tail"], e)
-    print(f"\n{cid}: worst O {worst['o']:.4g} L {worst['l']:.3g} dQ-rows {worst['dq']:.3g} dK/dV {worst['dkdv_tail']:.3g}")
+        worst["dq_rows"] = max(worst["dq_rows"], e)
+
+    # whole heads: dQ, dK, dV of every row; O and L of every row of the first and last head
+    for h in _whole_heads(BH, N):
+        x = x_of(h)
+        if h in (0, BH - 1):
+            o_r, l_r, _ = oracle.attn_rows(x["q"], x["k"], x["v"], np.arange(N, dtype=np.int64), scale, causal)
+            err = np.abs(og[h] - o_r)
+            assert np.all(err <= o_tolerance(o_r, dtype)), (h, "whole-head O", float(err.max()))
+            worst["o"] = max(worst["o"], float(err.max()))
+            le = float(np.max(np.abs(lg[h] - l_r)))
+            assert le <= TOL_L_MAXABS, (h, "whole-head L", le)
+            worst["l"] = max(worst["l"], le)
+        dq_r, dk_r, dv_r = _whole_head_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, threads)
+        errs = {}
+        for name, got, ref in (("dq", dqg[h], dq_r), ("dk", dkg[h], dk_r), ("dv", dvg[h], dv_r)):
+            errs[name] = rel_fro(got, ref)
+            worst[name] = max(worst[name], errs[name])
+        per_head.append((h, errs))
+        for name, e in errs.items():
+            assert e <= TOL_GRAD_RELFRO, (h, name, "whole head", e)
+    print(f"\n{cid}: worst O max-abs {worst['o']:.4g}, L max-abs {worst['l']:.3g}, dQ rows {worst['dq_rows']:.3g}; "
+          f"whole heads rel. Frobenius dQ {worst['dq']:.3g} dK {worst['dk']:.3g} dV {worst['dv']:.3g} "
+          f"(heads {[h for h, _ in per_head]})")
 
 
 def test_largest_supported_size(attn):

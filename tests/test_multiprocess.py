@@ -46,3 +46,20 @@ def test_two_gloo_ranks_take_the_max_step_time():
     assert [o[0] for o in out] == [0, 1]
     assert all(o[1] == 2 for o in out)
     assert all(o[3] == 11.0 for o in out)   # max over ranks of 10 + rank
+
+
+def test_bench_gpus_flag_starts_the_ranks_itself():
+    """`bench.py --gpus 2` without an outer launcher starts two ranks through
+    torch.distributed.run (gloo rendezvous on 127.0.0.1).  The oracle arm runs on CPU, so the
+    spawn path is exercised here without a GPU: rank 0 prints one line that reports both
+    ranks, the other rank exits 0 without work."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2",
+                          "--steps", "1", "--warmup", "3"], env=env, capture_output=True, text=True, timeout=600)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, out.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0

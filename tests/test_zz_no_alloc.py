@@ -5,7 +5,9 @@ that hands its plugins only their inputs and outputs, code that cannot accept
 cudaMalloc's implicit synchronisation) get a backward whose scratch is a fixed
 array inside the library.  These tests call it through the C ABI, twice in a
 row, and check its results against the workspace entry point attn_bwd within
-the parity tolerance; and check that a problem too large for the fixed array
+the parity tolerance and against the FP64 oracle directly; check that the
+device's free memory does not change across the second call (the array was
+reserved by the first); and check that a problem too large for the fixed array
 is refused before anything is queued.
 
 This file is collected last so that a run stopping at the first failure has
@@ -18,7 +20,8 @@ import os
 import numpy as np
 import pytest
 
-from attn_cases import TOL_GRAD_RELFRO, input_bits, rel_fro, to_device, to_f64
+import oracle
+from attn_cases import TOL_GRAD_RELFRO, f64, input_bits, rel_fro, to_device, to_f64
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -54,20 +57,30 @@ def test_noalloc_matches_workspace_entry_point(lib, B, H, N, d, causal, dtype):
     scale = 1.0 / math.sqrt(d)
     o, lse = attn.forward(q, k, v, scale, causal)
     ref = [to_f64(t) for t in attn.backward(q, k, v, o, do, lse, scale, causal)]
+    shp = (B, H, N, d)
+    exact = oracle.attn_bwd(*(f64(bits[n], dtype).reshape(shp) for n in ("q", "k", "v", "do")), scale, causal)
     code = 0 if dtype == "bf16" else 1
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for call in range(2):
         dq, dk, dv = (torch.full_like(q, float("nan")) for _ in range(3))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         st = clib.attn_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
                                    _ptr(dv), B, H, N, d, scale, int(causal), code, stream)
         assert st == 0, attn.attn_status_string(st)
         torch.cuda.synchronize()
+        free_after = torch.cuda.mem_get_info()[0]
         assert attn.attn_last_device_error() == 0
+        if call == 1:
+            # the scratch array was reserved with the first call's module load; later calls reserve nothing
+            assert free_after == free_before, (free_before, free_after)
         for name, got, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
             g = to_f64(got)
             assert np.isfinite(g).all(), (call, name)
             e = rel_fro(g, r)
-            assert e <= TOL_GRAD_RELFRO, (call, name, e)
+            assert e <= TOL_GRAD_RELFRO, (call, name, "vs attn_bwd", e)
+            e = rel_fro(g, exact[name])
+            assert e <= TOL_GRAD_RELFRO, (call, name, "vs the oracle", e)
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(lib):
