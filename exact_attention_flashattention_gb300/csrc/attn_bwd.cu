@@ -519,15 +519,23 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             // d = 128: dQ_i^T = K_j^T dS^T (A = K_j read MN-major, B = dS^T MN-major).
             // d = 64:  dQ_i = dS K_j (A = dS^T read MN-major, B = K_j MN-major).
             // Reads the dS tile in shared memory; writes the dP^T columns (dK has read dS^T there).
+            const uint64_t kd_mn = sdesc_sw128(k_base, kPanelBytes, 1024);
+            const uint64_t sd_mn = sdesc_sw128(ds_base, kPanelBytes, 1024);
             auto issue_dq = [&]() {
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t kd = sdesc_sw128(k_base + kk * 2048, kPanelBytes, 1024);
-                    const uint64_t sd = sdesc_sw128(ds_base + kk * 2048, kPanelBytes, 1024);
-                    if constexpr (D == 128) warp_mma_ss(tmem + L::kTmemDQ, kd, sd, kIdescQ, kk > 0);
-                    else warp_mma_ss(tmem + L::kTmemDQ, sd, kd, kIdescQ, kk > 0);
-                }
+                if constexpr (D == 128)
+                    warp_mma_ss8<GB300_MNMAJ_OFFS, GB300_MNMAJ_OFFS>(tmem + L::kTmemDQ, kd_mn, sd_mn, kIdescQ, 0);
+                else
+                    warp_mma_ss8<GB300_MNMAJ_OFFS, GB300_MNMAJ_OFFS>(tmem + L::kTmemDQ, sd_mn, kd_mn, kIdescQ, 0);
                 warp_mma_commit(&bars[L::kBarDqFull]);
+            };
+            // S^T = K_j Q_i^T and dP^T = V_j dO_i^T: K-major operands, D / 16 steps
+            auto issue_kmajor = [&](uint32_t d_col, uint32_t a_base, uint32_t b_base) {
+                const uint64_t ad = sdesc_sw128(a_base, 16, 1024), bd = sdesc_sw128(b_base, 16, 1024);
+                if constexpr (D == 128)
+                    warp_mma_ss8<GB300_KMAJ_OFFS(kPanelBytes), GB300_KMAJ_OFFS(kPanelBytes)>(tmem + d_col, ad, bd,
+                                                                                          kIdescS, 0);
+                else
+                    warp_mma_ss4<2, 4, 6, 2, 4, 6>(tmem + d_col, ad, bd, kIdescS, 0);
             };
             BwdUnits<kDyn> units(n_units);
             for (int u; ok && (u = units.template next<L>(bars, guard, kDevTimeoutMma)) >= 0;) {
@@ -542,13 +550,7 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         const uint32_t sst = gg & 1;
                         if (!warp_mbar_wait(&bars[L::kBarQFull + sst], (gg >> 1) & 1, guard, kDevTimeoutMma)) return false;
                         tc_fence_after();
-                        const uint32_t sqs = q_base + sst * L::kTile;
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            warp_mma_ss(tmem + L::kTmemS, sdesc_sw128(k_base + off, 16, 1024),
-                                   sdesc_sw128(sqs + off, 16, 1024), kIdescS, kk > 0);
-                        }
+                        issue_kmajor(L::kTmemS, k_base, q_base + sst * L::kTile);
                         warp_mma_commit(&bars[L::kBarSFull]);
                         return true;
                     };
@@ -571,34 +573,21 @@ attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         // dP^T = V_j dO_i^T, once the previous dQ tile has left these columns
                         if (!warp_mbar_wait(&bars[L::kBarDqFree], (g & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                            warp_mma_ss(tmem + L::kTmemDP, sdesc_sw128(v_base + off, 16, 1024),
-                                   sdesc_sw128(dos + off, 16, 1024), kIdescS, kk > 0);
-                        }
+                        issue_kmajor(L::kTmemDP, v_base, dos);
                         warp_mma_commit(&bars[L::kBarDpFull]);
                         if (it == w.n - 1) warp_mma_commit(&bars[L::kBarVEmpty]);
                         // dV += P^T dO_i
                         if (!warp_mbar_wait(&bars[L::kBarPReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         if (it == 0 && !warp_mbar_wait(&bars[L::kBarDkvEmpty], (k & 1) ^ 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                            warp_mma_ts(tmem + L::kTmemDV, tmem + L::kTmemS + acol,
-                                   sdesc_sw128(dos + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        warp_mma_ts8<GB300_TMEM_A_OFFS, GB300_MNMAJ_OFFS>(
+                            tmem + L::kTmemDV, tmem + L::kTmemS, sdesc_sw128(dos, kPanelBytes, 1024), kIdescG, it > 0);
                         if (!kDqAfterS && it + 1 < w.n && !issue_s(g + 1)) { ok = false; break; }
                         // dK += dS^T Q_i
                         if (!warp_mbar_wait(&bars[L::kBarDsReady], g & 1, guard, kDevTimeoutMma)) { ok = false; break; }
                         tc_fence_after();
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t acol = 64 * (kk >> 2) + 8 * (kk & 3);
-                            warp_mma_ts(tmem + L::kTmemDK, tmem + L::kTmemDP + acol,
-                                   sdesc_sw128(qs + kk * 2048, kPanelBytes, 1024), kIdescG, (it > 0 || kk > 0) ? 1u : 0u);
-                        }
+                        warp_mma_ts8<GB300_TMEM_A_OFFS, GB300_MNMAJ_OFFS>(
+                            tmem + L::kTmemDK, tmem + L::kTmemDP, sdesc_sw128(qs, kPanelBytes, 1024), kIdescG, it > 0);
                         warp_mma_commit(&bars[L::kBarQEmpty + st]);
                         if (!kDqAfterS) issue_dq();
                     }

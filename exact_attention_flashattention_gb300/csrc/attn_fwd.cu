@@ -451,24 +451,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             const uint32_t kv_base = smem_u32(smem + L::kKV);
             uint32_t tok = 0, q_phase = 0, pv_phase[2] = {0, 0};
             bool ok = true;
+            // S_q = Q_q K^T (K-major operands, D / 16 steps) and O_q += P_q V (P packed in S_q's
+            // first 64 columns, 8 columns per step; V read MN-major), each one chain of MMAs.
             auto issue_qk = [&](int q, uint32_t slot) {
                 const uint32_t d_tmem = tmem + L::kTmemS + 128 * q;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-                    const uint64_t a = sdesc_sw128(q_base[q] + off, 16, 1024);
-                    const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + off, 16, 1024);
-                    warp_mma_ss(d_tmem, a, b, kIdescQK, kk > 0);
-                }
+                const uint64_t a = sdesc_sw128(q_base[q], 16, 1024);
+                const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile, 16, 1024);
+                if constexpr (D == 128)
+                    warp_mma_ss8<GB300_KMAJ_OFFS(kPanelBytes), GB300_KMAJ_OFFS(kPanelBytes)>(d_tmem, a, b, kIdescQK, 0);
+                else
+                    warp_mma_ss4<2, 4, 6, 2, 4, 6>(d_tmem, a, b, kIdescQK, 0);
             };
             auto issue_pv = [&](int q, uint32_t slot, bool acc) {
                 const uint32_t d_tmem = tmem + L::kTmemO + 128 * q;
                 const uint32_t p_tmem = tmem + L::kTmemS + 128 * q;
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile + kk * 2048, kPanelBytes, 1024);
-                    warp_mma_ts(d_tmem, p_tmem + kk * 8, b, kIdescPV, (acc || kk > 0) ? 1u : 0u);
-                }
+                const uint64_t b = sdesc_sw128(kv_base + slot * L::kTile, kPanelBytes, 1024);
+                warp_mma_ts8<8, 16, 24, 32, 40, 48, 56, GB300_MNMAJ_OFFS>(d_tmem, p_tmem, b, kIdescPV, acc ? 1u : 0u);
             };
             auto wait_kv = [&](uint32_t& slot) -> bool {
                 slot = tok % L::kStages;

@@ -187,6 +187,86 @@ __device__ __forceinline__ void warp_mma_commit(uint64_t* bar) {
         ::"r"(smem_u32(bar)) : "memory");
 }
 
+// One product of several K steps (a chain of tcgen05.mma into the same accumulator) from a
+// single asm block: the lane-0 test and the enable-input-d predicates are set once, and every
+// later step's shared-memory descriptor is the first one plus a constant added to its low word
+// (only the start-address field changes, and it cannot carry out of its 14 bits inside the
+// 256 KB shared window).  Offsets are in descriptor units (bytes >> 4).  The per-instruction
+// work of the issuing warp is then an add or two and the MMA itself, which matters because the
+// MMA warp shares its scheduler with busy elementwise warps.  The first step accumulates when
+// acc_first != 0, the later ones always.
+#define GB300_MMA_PRE                                                                                  \
+    "{\n\t.reg .pred e, p, t;\n\t.reg .b32 l, alo, blo;\n\t.reg .b64 a, b;\n\t"                         \
+    "mov.u32 l, %%laneid;\n\tsetp.eq.u32 e, l, 0;\n\tsetp.ne.b32 p, %6, 0;\n\tsetp.eq.u32 t, l, l;\n\t"
+// SS step: A and B descriptors {lo + off, hi}
+#define GB300_MMA_SS_STEP(ao, bo)                                                                      \
+    "add.u32 alo, %1, %" #ao ";\n\tadd.u32 blo, %3, %" #bo ";\n\t"                                     \
+    "mov.b64 a, {alo, %2};\n\tmov.b64 b, {blo, %4};\n\t"                                               \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, t;\n\t"
+// TS step: A in TMEM at %1 + ao (columns), B descriptor {lo + off, hi}
+#define GB300_MMA_TS_STEP(ao, bo)                                                                      \
+    "add.u32 alo, %1, %" #ao ";\n\tadd.u32 blo, %3, %" #bo ";\n\t"                                     \
+    "mov.b64 b, {blo, %4};\n\t"                                                                        \
+    "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [alo], b, %5, t;\n\t"
+
+template <int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B1, int B2, int B3, int B4, int B5, int B6,
+          int B7>
+__device__ __forceinline__ void warp_mma_ss8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc_first) {
+    asm volatile(GB300_MMA_PRE
+                 "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t"
+                 GB300_MMA_SS_STEP(7, 14) GB300_MMA_SS_STEP(8, 15) GB300_MMA_SS_STEP(9, 16)
+                 GB300_MMA_SS_STEP(10, 17) GB300_MMA_SS_STEP(11, 18) GB300_MMA_SS_STEP(12, 19)
+                 GB300_MMA_SS_STEP(13, 20) "}"
+                 ::"r"(d_tmem), "r"((uint32_t)a_desc), "r"((uint32_t)(a_desc >> 32)), "r"((uint32_t)b_desc),
+                 "r"((uint32_t)(b_desc >> 32)), "r"(idesc), "r"(acc_first),
+                 "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7),
+                 "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+                 : "memory");
+}
+template <int A1, int A2, int A3, int B1, int B2, int B3>
+__device__ __forceinline__ void warp_mma_ss4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc_first) {
+    asm volatile(GB300_MMA_PRE
+                 "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %5, p;\n\t"
+                 GB300_MMA_SS_STEP(7, 10) GB300_MMA_SS_STEP(8, 11) GB300_MMA_SS_STEP(9, 12) "}"
+                 ::"r"(d_tmem), "r"((uint32_t)a_desc), "r"((uint32_t)(a_desc >> 32)), "r"((uint32_t)b_desc),
+                 "r"((uint32_t)(b_desc >> 32)), "r"(idesc), "r"(acc_first),
+                 "n"(A1), "n"(A2), "n"(A3), "n"(B1), "n"(B2), "n"(B3)
+                 : "memory");
+}
+template <int A1, int A2, int A3, int A4, int A5, int A6, int A7, int B1, int B2, int B3, int B4, int B5, int B6,
+          int B7>
+__device__ __forceinline__ void warp_mma_ts8(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t acc_first) {
+    asm volatile(GB300_MMA_PRE
+                 "mov.b64 b, {%3, %4};\n\t"
+                 "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], b, %5, p;\n\t"
+                 GB300_MMA_TS_STEP(7, 14) GB300_MMA_TS_STEP(8, 15) GB300_MMA_TS_STEP(9, 16)
+                 GB300_MMA_TS_STEP(10, 17) GB300_MMA_TS_STEP(11, 18) GB300_MMA_TS_STEP(12, 19)
+                 GB300_MMA_TS_STEP(13, 20) "}"
+                 ::"r"(d_tmem), "r"(a_tmem), "r"(0u), "r"((uint32_t)b_desc), "r"((uint32_t)(b_desc >> 32)),
+                 "r"(idesc), "r"(acc_first),
+                 "n"(A1), "n"(A2), "n"(A3), "n"(A4), "n"(A5), "n"(A6), "n"(A7),
+                 "n"(B1), "n"(B2), "n"(B3), "n"(B4), "n"(B5), "n"(B6), "n"(B7)
+                 : "memory");
+}
+#undef GB300_MMA_PRE
+#undef GB300_MMA_SS_STEP
+#undef GB300_MMA_TS_STEP
+
+// Descriptor-unit offsets of the K steps of the two operand layouts used here:
+//  * K-major SW128, 64-column panels kPanel bytes apart: step kk starts (kk / 4) panels and
+//    (kk % 4) x 32 bytes in;
+//  * MN-major SW128: step kk starts 16 rows = 2048 bytes further.
+// and the TMEM column offsets of a packed 16-bit A operand (8 columns per K step), for the two
+// 64-row halves of the key / query index written at columns 0 and 64.
+#define GB300_KMAJ_OFFS(panel) 2, 4, 6, (panel) / 16, (panel) / 16 + 2, (panel) / 16 + 4, (panel) / 16 + 6
+#define GB300_MNMAJ_OFFS 128, 256, 384, 512, 640, 768, 896
+#define GB300_TMEM_A_OFFS 8, 16, 24, 64, 72, 80, 88
+
 // Instruction descriptor, kind::f16 with FP32 accumulation (PTX ISA,
 // "Instruction descriptor"): D format bits [4,6), A format [7,10), B format
 // [10,13), A major bit 15, B major bit 16 (1 = MN-major), N>>3 at [17,23),
