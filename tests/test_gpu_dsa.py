@@ -138,10 +138,11 @@ def _sub_bwd(x, rows, idx_rows, scale, causal):
                           t(x["sink"]), idx_rows, None, scale, causal, 512)
 
 
-def _forward_inputs(x, scale, d_v=512):
+def _forward_inputs(x, scale, d_v=512, causal=False):
     """The backward's O (bf16) and L (FP32) inputs at full size, from a plain PyTorch FP32
     forward over each row's gathered keys with the sink in the denominator (input
-    preparation: the oracle's backward is given these same O and L)."""
+    preparation: the oracle's backward is given these same O and L).  causal: entries naming
+    a key after the row's own position take no part."""
     q, kv, sink, idx = x["q"], x["kv"], x["sink"], x["idx"]
     s_q, H = q.shape[0], q.shape[1]
     o = torch.empty((s_q, H, d_v), dtype=torch.bfloat16, device="cuda")
@@ -152,7 +153,10 @@ def _forward_inputs(x, scale, d_v=512):
         ix = idx[r0:r1].long()
         K = kvf[ix.clamp(min=0)]
         S = torch.einsum("rhd,rkd->rhk", q[r0:r1].float(), K) * scale
-        S = S.masked_fill(~(ix >= 0)[:, None, :], float("-inf"))
+        valid = ix >= 0
+        if causal:
+            valid &= ix <= torch.arange(r0, r1, device="cuda")[:, None]
+        S = S.masked_fill(~valid[:, None, :], float("-inf"))
         L = torch.logsumexp(torch.cat([S, sink[None, :, None].expand(r1 - r0, H, 1)], dim=2), dim=2)
         o[r0:r1] = torch.einsum("rhk,rkd->rhd", torch.exp(S - L[:, :, None]), K[:, :, :d_v]).to(torch.bfloat16)
         lse[r0:r1] = L
@@ -198,6 +202,58 @@ def test_dsa_bwd_full_size_sampled(attn):
             one = np.full((len(part), 1), j, dtype=np.int32)
             ref_j += _sub_bwd(x, part.tolist(), one, scale, False)["dkv"][j]
         assert rel_fro(got_kv[j], ref_j) <= TOL_GRAD_RELFRO, ("dkv", j)
+
+    dsink_ref = np.zeros(H)
+    empty = np.full((256, 1), -1, dtype=np.int32)
+    for r0 in range(0, s, 256):
+        dsink_ref += _sub_bwd(x, list(range(r0, r0 + 256)), empty, scale, False)["dsink"]
+    assert rel_fro(dsink.cpu().numpy().astype(np.float64), dsink_ref) <= TOL_DSINK
+
+
+def test_dsa_bwd_full_size_causal_sampled(attn):
+    """s_q = s_kv = 4096, H = 64, QK = V = 512, top-k 2048, sink on, causal: every row's list
+    is drawn from all 4096 keys, so the kernel must mask the entries after the row's own
+    position.  The oracle gets each sampled row's list with those entries replaced by -1
+    (its reading of an invalid entry), which is the causal computation for that row.  dQ on
+    sampled rows (early rows, where most entries are masked, and late ones); dKV on sampled
+    keys from the rows at or after them that list them; dSink over all rows."""
+    s, H, d_qk, topk = 4096, 64, 512, 2048
+    x = si.dsa_device_draws(s, s, H, d_qk, topk, False, seed=23)
+    scale = d_qk ** -0.5
+    x["o"], x["lse"] = _forward_inputs(x, scale, causal=True)
+    dq = torch.full_like(x["q"], float("nan"))
+    dkv = torch.full_like(x["kv"], float("nan"))
+    dsink = torch.full_like(x["sink"], float("nan"))
+    ws = torch.empty(attn.attn_dsa_bwd_workspace_size(s, d_qk), dtype=torch.uint8, device="cuda")
+    attn.attn_dsa_bwd(x["q"], x["kv"], x["o"], x["do"], x["lse"], x["sink"], x["idx"], x["lens"], dq, dkv, dsink, ws,
+                      scale, True)
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+    assert torch.isfinite(dq.float()).all() and torch.isfinite(dkv.float()).all()
+    idx = x["idx"].cpu().numpy()
+    later = idx > np.arange(s)[:, None]
+    idx_causal = np.where(later, -1, idx).astype(np.int32)
+    rng = np.random.default_rng(5)
+
+    rows = [0, 1, 7, 130, 2047, s - 1] + [int(r) for r in rng.integers(0, s, 4)]
+    ref = _sub_bwd(x, rows, idx_causal[rows], scale, False)
+    got = dq[torch.as_tensor(rows, device="cuda")].float().cpu().numpy().astype(np.float64)
+    for n, r in enumerate(rows):
+        e = rel_fro(got[n], ref["dq"][n]) if np.any(ref["dq"][n]) else float(np.max(np.abs(got[n])))
+        assert e <= TOL_GRAD_RELFRO, ("dq", r, e)
+
+    got_kv = dkv.float().cpu().numpy().astype(np.float64)
+    for j in [0, 1, s // 2, s - 1] + [int(k) for k in rng.integers(0, s, 2)]:
+        q_rows = np.nonzero((idx_causal == j).any(axis=1))[0]
+        ref_j = np.zeros(d_qk)
+        for c0 in range(0, len(q_rows), 256):
+            part = q_rows[c0:c0 + 256]
+            one = np.full((len(part), 1), j, dtype=np.int32)
+            ref_j += _sub_bwd(x, part.tolist(), one, scale, False)["dkv"][j]
+        if np.any(ref_j):
+            assert rel_fro(got_kv[j], ref_j) <= TOL_GRAD_RELFRO, ("dkv", j)
+        else:
+            assert np.max(np.abs(got_kv[j])) == 0.0, ("dkv of a key no row may use", j)
 
     dsink_ref = np.zeros(H)
     empty = np.full((256, 1), -1, dtype=np.int32)
