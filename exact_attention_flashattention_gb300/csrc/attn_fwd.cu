@@ -190,6 +190,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float* __restrict__ lse_out, const SeqDesc seq, float scale, int causal,
                 unsigned int* __restrict__ sched, int* error) {
     using L = FwdLayout<D>;
+    // K/V ring tokens come in the order K_0, then V_j, K_{j+1} per step (V_{n-1}, K_0 of the next
+    // item at an item boundary).  With the static work list the loader knows where the work ends,
+    // so it signals each (V_j, following K) pair on one barrier, that of V_j's slot, and the MMA
+    // warp takes one wait per step instead of two.
+    constexpr bool kPairKV = !kDyn;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align the dynamic shared memory base to 1024 bytes (128B-swizzle atoms).
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -481,7 +486,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 q_phase ^= 1;
                 tc_fence_after();
                 uint32_t kslot;
-                if (!wait_kv(kslot)) { ok = false; break; }
+                if (kPairKV && tok > 0) {
+                    kslot = tok++ % L::kStages;  // landed with the previous item's last V
+                } else if (!wait_kv(kslot)) {
+                    ok = false;
+                    break;
+                }
                 issue_qk(0, kslot);
                 warp_mma_commit(&bars[L::kBarSFull + 0]);
                 issue_qk(1, kslot);
@@ -493,7 +503,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 if (w.n1 == 1) warp_mma_commit(&bars[L::kBarQEmpty]);
                 for (int j = 0; j < w.n1 && ok; ++j) {
                     uint32_t vslot;
-                    if (!wait_kv(vslot)) { ok = false; break; }
+                    if (!wait_kv(vslot)) { ok = false; break; }  // kPairKV: V_j and the K after it
                     bool have_k = false;
 #pragma unroll
                     for (int q = 0; q < 2; ++q) {
@@ -506,7 +516,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         warp_mma_commit(&bars[L::kBarODone + q]);
                         if (j + 1 < n) {
                             if (!have_k) {
-                                if (!wait_kv(kslot)) { ok = false; break; }
+                                if (kPairKV) kslot = tok++ % L::kStages;
+                                else if (!wait_kv(kslot)) { ok = false; break; }
                                 have_k = true;
                             }
                             issue_qk(q, kslot);
@@ -546,8 +557,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             uint32_t tok = 0;
             bool ok = true;
             WorkItem w;
-            for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad);) {
-                for (int j = 0; j < w.n1 && ok; ++j) {
+            FwdIter<kDyn> itr;
+            bool more = itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad);
+            while (ok && more) {
+                const WorkItem cur = w;
+                // kPairKV: whether a K follows this item's last V (the static list is read one item
+                // ahead; the dynamic one is not, its next unit is taken only when needed)
+                if constexpr (kPairKV) more = itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad);
+                for (int j = 0; j < cur.n1 && ok; ++j) {
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = tok % L::kStages;
@@ -556,19 +573,33 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                             ok = false;
                             break;
                         }
-                        mbar_arrive_expect_tx(&bars[L::kBarKVFull + slot], L::kTile);
+                        // the barrier this tile lands on: its own, or (kPairKV, a K after the first
+                        // token) that of the V before it, which expects both tiles
+                        uint32_t fslot = slot;
+                        if (!kPairKV || tok == 0) {
+                            mbar_arrive_expect_tx(&bars[L::kBarKVFull + slot], L::kTile);
+                        } else if (tok & 1) {
+                            const bool pair = more || j + 1 < cur.n1;
+                            mbar_arrive_expect_tx(&bars[L::kBarKVFull + slot], pair ? 2 * L::kTile : L::kTile);
+                        } else {
+                            fslot = (tok - 1) % L::kStages;
+                        }
                         const CUtensorMap* map = which ? &tm_v : &tm_k;
 #pragma unroll
                         for (int p = 0; p < L::kPanels; ++p)
                             seq_tma_load<kTM>(smem + L::kKV + slot * L::kTile + p * kPanelBytes, map,
-                                         &bars[L::kBarKVFull + slot], w.si, 64 * p, j * 128);
+                                         &bars[L::kBarKVFull + fslot], cur.si, 64 * p, j * 128);
                         ++tok;
                     }
                 }
+                if (!ok) break;
+                if constexpr (!kPairKV) more = itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutLoad);
             }
-            // Let every copy issued above land before shared memory is released.
+            // Let every copy issued above land before shared memory is released (kPairKV: the
+            // second tile of a pair lands on the first one's barrier).
             for (uint32_t t = (tok > (uint32_t)L::kStages ? tok - L::kStages : 0); t < tok; ++t)
-                mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
+                if (!kPairKV || t == 0 || (t & 1))
+                    mbar_wait_drain(&bars[L::kBarKVFull + t % L::kStages], (t / L::kStages) & 1, kWaitLimitNs);
         } else if (kDyn && warp == 15 && lane == 0) {
             // ------------------------------------------------------------ scheduler
             // It waits with a sleep between polls: its warp shares a scheduler with softmax warps.
