@@ -193,7 +193,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     // K/V ring tokens come in the order K_0, then V_j, K_{j+1} per step (V_{n-1}, K_0 of the next
     // item at an item boundary).  With the static work list the loader knows where the work ends,
     // so it signals each (V_j, following K) pair on one barrier, that of V_j's slot, and the MMA
-    // warp takes one wait per step instead of two.
+    // warp takes one wait per step instead of two.  The pair is released the same way, with one
+    // commit on V_j's empty barrier once both tiles have been read (for V_{n-1}, K_0 of the next
+    // item: after that item's first S products); the loader waits on it for both slots.
     constexpr bool kPairKV = !kDyn;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Align the dynamic shared memory base to 1024 bytes (128B-swizzle atoms).
@@ -480,6 +482,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tc_fence_after();
                 return r;
             };
+            int pending = -1;  // kPairKV: slot of a V whose pair ends with the next item's K_0
             WorkItem w;
             for (FwdIter<kDyn> itr; ok && itr.template next<kTM, L>(w, M, causal, seq, n_units, bars, guard, kDevTimeoutMma);) {
                 if (!warp_mbar_wait(&bars[L::kBarQFull], q_phase, guard, kDevTimeoutMma)) { ok = false; break; }
@@ -496,7 +499,8 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 warp_mma_commit(&bars[L::kBarSFull + 0]);
                 issue_qk(1, kslot);
                 warp_mma_commit(&bars[L::kBarSFull + 1]);
-                warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                warp_mma_commit(&bars[L::kBarKVEmpty + (kPairKV && pending >= 0 ? (uint32_t)pending : kslot)]);
+                pending = -1;
                 // Q is read by the S MMAs only: the Q buffers are released after the item's last
                 // S (S_1(n1 - 1); S_0's last comes no later), so that the next item's Q loads
                 // while this item's last PVs and epilogue run.
@@ -526,10 +530,16 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                         }
                     }
                     if (!ok) break;
-                    warp_mma_commit(&bars[L::kBarKVEmpty + vslot]);
-                    if (have_k) warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                    if constexpr (kPairKV) {
+                        if (have_k) warp_mma_commit(&bars[L::kBarKVEmpty + vslot]);
+                        else pending = (int)vslot;  // released after the next item's K_0 is read
+                    } else {
+                        warp_mma_commit(&bars[L::kBarKVEmpty + vslot]);
+                        if (have_k) warp_mma_commit(&bars[L::kBarKVEmpty + kslot]);
+                    }
                 }
             }
+            if (kPairKV && pending >= 0) warp_mma_commit(&bars[L::kBarKVEmpty + pending]);
             // Every MMA issued above completes before TMEM is released.
             warp_mma_commit(&bars[L::kBarTeardown]);
             mbar_wait_drain(&bars[L::kBarTeardown], 0, kWaitLimitNs);
@@ -568,7 +578,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
                     for (int which = 0; which < 2; ++which) {
                         const uint32_t slot = tok % L::kStages;
-                        if (tok >= (uint32_t)L::kStages &&
+                        // the previous tile in this slot must have been read.  kPairKV: a pair's
+                        // first slot waits for the release of the pair there before (both slots),
+                        // a second slot only where it last held the lone first K (token 0).
+                        const bool wait_empty = tok >= (uint32_t)L::kStages &&
+                                                (!kPairKV || (tok & 1) || tok == (uint32_t)L::kStages);
+                        if (wait_empty &&
                             !mbar_wait(&bars[L::kBarKVEmpty + slot], ((tok / L::kStages) - 1) & 1, guard, kDevTimeoutLoad)) {
                             ok = false;
                             break;
