@@ -27,6 +27,7 @@ BSHD_CASES = [
     (1, 2, 512, 128, False, "bf16"),
     (2, 2, 77, 64, True, "bf16"),
     (1, 2, 256, 64, False, "fp16"),
+    (2, 100, 200, 64, True, "bf16"),  # 200 units: several items per CTA, ragged tiles
 ]
 DQ_CROSS = 2e-3
 PACKED_CASES = [

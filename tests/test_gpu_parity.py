@@ -36,6 +36,12 @@ SMALL = [
     (1, 2, 333, 128, True, "bf16"),
     (2, 1, 257, 128, True, "fp16"),
     (1, 2, 1000, 64, False, "fp16"),
+    # more work units than SMs, so a CTA runs several items and the forward's K/V pairs span
+    # item boundaries (a V with the next item's first K): one key tile per item, two, and an
+    # odd tile count
+    (1, 400, 128, 64, False, "bf16"),
+    (1, 200, 256, 128, True, "bf16"),
+    (2, 160, 384, 64, True, "fp16"),
 ]
 
 
