@@ -608,6 +608,7 @@ def run_sweep(iters=100, warmup=20):
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream(dev)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
     for name, B, H, N, d, causal, dtype, sig in SWEEP:
         tdt = torch.bfloat16 if dtype == "bf16" else torch.float16
         g = torch.Generator(device=dev)
@@ -622,16 +623,24 @@ def run_sweep(iters=100, warmup=20):
         def timed(fn):
             return time_calls(fn, stream, iters, warmup)
 
+        clk = ClockSampler(torch.cuda.current_device())
+        clk.start()
         fms = timed(lambda: attn.attn_fwd(q, k, v, o, lse, sc, causal, stream))
         bms = timed(lambda: attn.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, sc, causal, stream))
+        clocks = clk.stop()
         if attn.attn_last_device_error(stream) != 0:
             raise RuntimeError("device error word set")
         ftf = F.fwd_flops(B, H, N, d, causal) / fms / 1e9
         btf = F.bwd_flops(B, H, N, d, causal) / bms / 1e9
-        print(json.dumps({"sweep": name, "dtype": dtype, "fwd_ms": fms, "fwd_tflops": ftf,
-                          "fwd_pct_peak": 100 * ftf / burst, "bwd_ms": bms, "bwd_tflops": btf,
-                          "bwd_pct_peak": 100 * btf / burst, "peak_basis": f"bf16 burst {burst} ({src})"}),
-              flush=True)
+        line = {"sweep": name, "dtype": dtype, "fwd_ms": fms, "fwd_tflops": ftf, "bwd_ms": bms, "bwd_tflops": btf,
+                "fwd_pct_burst_peak": 100 * ftf / burst, "bwd_pct_burst_peak": 100 * btf / burst,
+                "burst_peak_basis": f"bf16 burst {burst} ({src})"}
+        if clocks:
+            nominal = nominal_bf16_tflops(n_sm, clocks["sm_mhz"])
+            line.update({"fwd_pct_at_clock": 100 * ftf / nominal, "bwd_pct_at_clock": 100 * btf / nominal,
+                         "clock_basis": f"{n_sm} SMs x {NOMINAL_FLOP_PER_CLK} FLOP/clk x {clocks['sm_mhz']:.0f} MHz "
+                                        f"(median sampled) = {nominal:.1f} TFLOP/s", "clocks": clocks})
+        print(json.dumps(line), flush=True)
         del q, k, v, do, o, lse, dq, dk, dv, ws
     # the same causal d = 128 work in the token-major layouts: BSHD, and 32 packed sequences of
     # lengths 512, 752, ..., 7952 (135424 tokens; most not a multiple of 128)
