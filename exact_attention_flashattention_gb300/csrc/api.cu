@@ -459,7 +459,7 @@ attn_status_t attn_decode(const void* q, const void* k_cache, const void* v_cach
     a.num_sms = di.sms;
     a.error = di.err_ptr;
     if (launch_decode(a, static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
-    t_last_launches = 2;
+    t_last_launches = a.splits > 1 ? 2 : 1;
     return ATTN_OK;
 }
 

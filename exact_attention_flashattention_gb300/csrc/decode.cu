@@ -94,8 +94,9 @@ template <int D, bool BF16>
 __global__ void __launch_bounds__(kDecThreads, 1)
 attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const int* __restrict__ seqlens,
-                   float* __restrict__ part_o, float* __restrict__ part_l, int Hkv, int G, int Nmax, int splits,
-                   int chunk, int n_items, float scale, int* error) {
+                   float* __restrict__ part_o, float* __restrict__ part_l, void* __restrict__ o_out,
+                   float* __restrict__ lse_out, int Hkv, int G, int Nmax, int splits, int chunk, int n_items,
+                   float scale, int* error) {
     using L = DecLayout<D>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -154,12 +155,20 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                 dec_item(u, splits, chunk, Hkv, Nmax, seqlens, error, threadIdx.x == 0, w);
                 float* po = part_o + (size_t)u * G * D;
                 float* pl = part_l + (size_t)u * G;
+                // one chunk per group: this item's result is the final one (query head u G + row),
+                // written here in 16 bits, and no combination kernel runs
+                uint8_t* od = static_cast<uint8_t*>(o_out) + ((size_t)u * G + row) * D * 2;
                 if (w.n_tiles == 0) {
-                    // empty chunk: weight exp(-inf) = 0 in the combination
+                    // empty chunk: weight exp(-inf) = 0 in the combination (an empty cache: O = 0, L = -inf)
                     if (row < G) {
-                        pl[row] = -INFINITY;
-                        for (int c = 0; c < D; c += 4)
-                            *reinterpret_cast<float4*>(po + (size_t)row * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (splits == 1) {
+                            for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(od + c * 2) = make_uint4(0, 0, 0, 0);
+                            lse_out[(size_t)u * G + row] = -INFINITY;
+                        } else {
+                            pl[row] = -INFINITY;
+                            for (int c = 0; c < D; c += 4)
+                                *reinterpret_cast<float4*>(po + (size_t)row * D + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
                     }
                     continue;
                 }
@@ -258,7 +267,15 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                     uint32_t r[32];
                     tmem_ld32(o_addr + c, r);
                     tmem_wait_ld();
-                    if (row < G) {
+                    if (row < G && splits == 1) {
+                        uint4* dst = reinterpret_cast<uint4*>(od + c * 2);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[e] = make_uint4(pack2<BF16>(__uint_as_float(r[8 * e]) * inv_l, __uint_as_float(r[8 * e + 1]) * inv_l),
+                                                pack2<BF16>(__uint_as_float(r[8 * e + 2]) * inv_l, __uint_as_float(r[8 * e + 3]) * inv_l),
+                                                pack2<BF16>(__uint_as_float(r[8 * e + 4]) * inv_l, __uint_as_float(r[8 * e + 5]) * inv_l),
+                                                pack2<BF16>(__uint_as_float(r[8 * e + 6]) * inv_l, __uint_as_float(r[8 * e + 7]) * inv_l));
+                    } else if (row < G) {
                         float4* dst = reinterpret_cast<float4*>(po + (size_t)row * D + c);
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
@@ -267,7 +284,11 @@ attn_decode_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
                                                  __uint_as_float(r[4 * e + 3]) * inv_l);
                     }
                 }
-                if (row < G) pl[row] = (m_run + log2f(l_run)) * kLn2;
+                if (row < G) {
+                    const float lrow = (m_run + log2f(l_run)) * kLn2;
+                    if (splits == 1) lse_out[(size_t)u * G + row] = lrow;
+                    else pl[row] = lrow;
+                }
                 tc_fence_before();
                 mbar_arrive(&bars[L::kBarOFree]);  // O may now be overwritten by the next item
                 gt += w.n_tiles;
@@ -483,13 +504,14 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         const long n_items = (long)a.groups * a.splits;
         const int grid = (int)(n_items < a.num_sms ? n_items : a.num_sms);
-        kern<<<grid, kDecThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.seqlens, a.part_o, a.part_l,
-                                                        a.Hkv, a.G, a.Nmax, a.splits, a.chunk, (int)n_items, a.scale,
-                                                        a.error);
+        kern<<<grid, kDecThreads, smem_bytes, stream>>>(a.tm_q, a.tm_k, a.tm_v, a.seqlens, a.part_o, a.part_l, a.o,
+                                                        a.lse, a.Hkv, a.G, a.Nmax, a.splits, a.chunk, (int)n_items,
+                                                        a.scale, a.error);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (a.stage < 0 || a.stage == 1) {
+    // with one chunk per group the chunk kernel has written O and L itself
+    if ((a.stage < 0 || a.stage == 1) && a.splits > 1) {
         const long rows = (long)a.groups * a.G;
         attn_decode_combine_kernel<D, BF16><<<(unsigned)rows, kCombThreads, 0, stream>>>(a.part_o, a.part_l, a.o,
                                                                                          a.lse, a.G, a.splits);

@@ -233,7 +233,9 @@ ATTN_API attn_status_t attn_bwd_noalloc(const void *q, const void *k, const void
  * other calls' limits, and a caller-owned `workspace` of at least
  * attn_decode_workspace_size() bytes, 256-byte aligned (the keys are split
  * into chunks processed in parallel; the workspace holds each chunk's partial
- * result).  Queues two kernels.
+ * result).  Queues two kernels: the chunk kernel and their combination, or
+ * the chunk kernel alone when the launch takes one chunk per (batch, KV head)
+ * (it then writes o and lse itself; attn_last_launch_count() says which).
  */
 ATTN_API size_t attn_decode_workspace_size(int B, int Hq, int Hkv, int Nmax, int d);
 ATTN_API attn_status_t attn_decode(const void *q, const void *k_cache, const void *v_cache, void *o,
