@@ -1,5 +1,5 @@
-// Fused attention backward for sm_103a: preprocess, main tcgen05 kernel and
-// dQ conversion ("Writing Speed-of-Light Attention Backward Kernel for 5090
+// Fused attention backward for sm_103a: the main tcgen05 kernel, launched between
+// the preprocess and the dQ conversion of bwd_aux.cu ("Writing Speed-of-Light Attention Backward Kernel for 5090
 // in CUDA", sections "Mathematical Formulation" and the tiled pseudocode that
 // follows it: one CTA owns dK_j and dV_j of a key/value tile j, loops over the
 // query tiles i it interacts with, and adds each dQ_i partial into an FP32
@@ -42,93 +42,6 @@ constexpr int kPanelBytes = 128 * 128;
 // d=64: 1500 / 2500 / 3000 / 3500 gave 0.586 / 0.562 / 0.518 / 0.516 ms against 0.592.
 template <int D>
 constexpr long long kDqPaceCycles = D == 128 ? 3000 : 3500;
-
-// ---------------------------------------------------------------- preprocess
-// ndelta_r = -scale * sum_c dO[r,c] O[r,c] (FP32: the negated D of the
-// backward equations, times the softmax scale that the main kernel folds into
-// dS), nlse2_r = -L_r log2(e), dq_acc[r,:] = 0.  The three workspace arrays
-// hold, per (sequence, head) slice, its rows padded to whole 128-row tiles
-// (seq_ws_base); the padding rows of a ragged last tile get nlse2 = -inf (so
-// P = 0 there) and ndelta = 0.  Threads walk (slice, row < n_pad) with n_pad
-// the padded length of the longest sequence and skip rows past a slice's own.
-template <int D, bool BF16, bool kTM>
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const uint4* __restrict__ o, const uint4* __restrict__ dout,
-                                                      const float* __restrict__ lse, float* __restrict__ delta,
-                                                      float* __restrict__ lse2, float4* __restrict__ dq_acc,
-                                                      const SeqDesc seq, int n_pad, float scale) {
-    constexpr int TPR = D / 8;
-    const long total = (long)seq.B * seq.H * n_pad * TPR;
-    const long stride = (long)gridDim.x * blockDim.x;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        const long prow = i / TPR;          // padded row of the longest sequence
-        const int part = (int)(i % TPR);
-        const int bh = (int)(prow / n_pad);
-        const int n = (int)(prow % n_pad);
-        SeqItem si;
-        seq_item<kTM>(seq, bh, si);
-        // the TPR threads of a row are consecutive lanes of one warp and take the same branches
-        if (n >= (si.len + 127) / 128 * 128) continue;
-        const size_t wrow = seq_ws_base<kTM>(seq, si, n_pad) + n;
-        const bool valid = n < si.len;
-        float acc = 0.f;
-        if (valid) {
-            const size_t src = seq_row_offset<kTM>(seq, si, n, D) / 8 + part;
-            const uint4 a = __ldg(o + src);
-            const uint4 b = __ldg(dout + src);
-            const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-            const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float2 fa, fb;
-                if constexpr (BF16) {
-                    fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
-                    fb = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&bv[e]));
-                } else {
-                    fa = __half22float2(*reinterpret_cast<const __half2*>(&av[e]));
-                    fb = __half22float2(*reinterpret_cast<const __half2*>(&bv[e]));
-                }
-                acc = fmaf(fa.x, fb.x, acc);
-                acc = fmaf(fa.y, fb.y, acc);
-            }
-        }
-        // The TPR lanes of a row (an aligned group: blocks are whole warps and total is a multiple
-        // of TPR) take every branch together, so the shuffle names exactly that group.
-        const unsigned lane = threadIdx.x & 31u;
-        const unsigned mask = (TPR >= 32) ? 0xffffffffu : (((1u << TPR) - 1u) << (lane & ~(unsigned)(TPR - 1)));
-#pragma unroll
-        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(mask, acc, off);
-        dq_acc[2 * (wrow * TPR + part)] = make_float4(0.f, 0.f, 0.f, 0.f);
-        dq_acc[2 * (wrow * TPR + part) + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (part == 0) {
-            delta[wrow] = valid ? -acc * scale : 0.f;
-            lse2[wrow] = valid ? -lse[seq_lse_index<kTM>(seq, si, n)] * kLog2e : -INFINITY;
-        }
-    }
-}
-
-// ---------------------------------------------------------------- dQ convert
-// dq row n of each (sequence, head) slice = 16-bit(its accumulator row), for n below the
-// sequence's length; threads walk (slice, row < N) with N the longest length.
-template <int D, bool BF16, bool kTM>
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float4* __restrict__ acc, uint4* __restrict__ dq,
-                                                         const SeqDesc seq, int n_pad) {
-    constexpr int PER_ROW = D / 8;   // 8 values (one uint4 of output) per thread
-    const long n8 = (long)seq.B * seq.H * seq.N * PER_ROW;
-    const long stride = (long)gridDim.x * blockDim.x;
-    for (long i = (long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += stride) {
-        const long row = i / PER_ROW;
-        const int part = (int)(i % PER_ROW);
-        const int bh = (int)(row / seq.N);
-        const int n = (int)(row % seq.N);
-        SeqItem si;
-        seq_item<kTM>(seq, bh, si);
-        if (n >= si.len) continue;
-        const size_t src = ((seq_ws_base<kTM>(seq, si, n_pad) + n) * PER_ROW + part) * 2;
-        const float4 a = acc[src], b = acc[src + 1];
-        dq[seq_row_offset<kTM>(seq, si, n, D) / 8 + part] =
-            make_uint4(pack2<BF16>(a.x, a.y), pack2<BF16>(a.z, a.w), pack2<BF16>(b.x, b.y), pack2<BF16>(b.z, b.w));
-    }
-}
 
 // ---------------------------------------------------------------- main kernel
 // Shared memory: K_j, V_j (one tile each), Q_i and dO_i (two stages each), dS
@@ -682,17 +595,9 @@ template <int D, bool BF16, bool kTM>
 cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
     using L = BwdLayout<D>;
     const int T = (a.N + 127) / 128;
-    const int N_pad = T * 128;
-    // 1. preprocess
+    // 1. preprocess (bwd_aux.cu)
     if (stage < 0 || stage == 0) {
-        const long threads_needed = (long)a.BH * N_pad * (D / 8);  // rows walked: every slice at the longest length
-        long blocks = (threads_needed + 255) / 256;
-        const long cap = (long)a.num_sms * 8;
-        if (blocks > cap) blocks = cap;
-        bwd_pre_kernel<D, BF16, kTM><<<(int)blocks, 256, 0, stream>>>(
-            static_cast<const uint4*>(a.o), static_cast<const uint4*>(a.dout), a.lse, a.delta, a.lse2,
-            reinterpret_cast<float4*>(a.dq_acc), a.seq, N_pad, a.scale);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_bwd_pre(a, stream);
         if (e != cudaSuccess) return e;
     }
     // 2. main kernel
@@ -719,15 +624,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, cudaStream_t stream, int stage) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    // 3. dQ conversion
+    // 3. dQ conversion (bwd_aux.cu)
     if (stage < 0 || stage == 2) {
-        const long n8 = (long)a.BH * a.N * (D / 8);
-        long blocks = (n8 + 255) / 256;
-        const long cap = (long)a.num_sms * 8;
-        if (blocks > cap) blocks = cap;
-        dq_convert_kernel<D, BF16, kTM><<<(int)blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(a.dq_acc),
-                                                                    static_cast<uint4*>(a.dq), a.seq, N_pad);
-        cudaError_t e = cudaGetLastError();
+        cudaError_t e = launch_dq_convert(a, stream);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;

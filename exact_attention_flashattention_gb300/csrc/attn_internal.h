@@ -118,5 +118,8 @@ cudaError_t launch_dsa_bwd(const DsaArgs& a, cudaStream_t stream);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 // stage: -1 = all three kernels; 0 = preprocess; 1 = main kernel; 2 = dQ conversion.
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t stream, int stage);
+// The backward's preprocess and dQ conversion kernels (bwd_aux.cu); launch_bwd calls them.
+cudaError_t launch_bwd_pre(const BwdArgs& a, cudaStream_t stream);
+cudaError_t launch_dq_convert(const BwdArgs& a, cudaStream_t stream);
 
 }  // namespace gb300
