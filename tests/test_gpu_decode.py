@@ -113,3 +113,27 @@ def test_decode_bad_cache_lengths_are_reported(attn):
     ref_o, ref_l = _reference(qb, kb, vb, B, Hq, Hkv, d, [100, 0, 0], dtype, scale)
     assert np.max(np.abs(got_o[0] - ref_o[0])) <= TOL_O_MAXABS
     assert np.max(np.abs(got_l[0] - ref_l[0])) <= TOL_L_MAXABS
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Nmax,d,launches", [
+    (2, 8, 2, 1000, 128, 1),    # one chunk per (batch, KV head): the chunk kernel writes O and L
+    (1, 16, 1, 2500, 128, 2),   # one group, three chunks: chunk kernel, then the combination
+])
+def test_decode_single_chunk_and_split_paths(attn, B, Hq, Hkv, Nmax, d, launches):
+    """Both ways a decode call ends, each against the oracle: with one key chunk per group the
+    chunk kernel's normalised O and L are the results (one launch); with several, a second
+    kernel combines the chunks."""
+    dtype = "bf16"
+    scale = 1.0 / math.sqrt(d)
+    qb, kb, vb = _inputs(8100 + Nmax, B, Hq, Hkv, Nmax, d, dtype)
+    q, k, v = _dev(qb, (B, Hq, d), dtype), _dev(kb, (B, Hkv, Nmax, d), dtype), _dev(vb, (B, Hkv, Nmax, d), dtype)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, Hq), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.empty(attn.attn_decode_workspace_size(B, Hq, Hkv, Nmax, d), dtype=torch.uint8, device="cuda")
+    attn.attn_decode(q, k, v, o, lse, ws, scale, None)
+    assert attn.attn_last_launch_count() == launches
+    torch.cuda.synchronize()
+    assert attn.attn_last_device_error() == 0
+    ref_o, ref_l = _reference(qb, kb, vb, B, Hq, Hkv, d, [Nmax] * B, dtype, scale)
+    assert np.max(np.abs(to_f64(o) - ref_o)) <= TOL_O_MAXABS
+    assert np.max(np.abs(to_f64(lse) - ref_l)) <= TOL_L_MAXABS
