@@ -179,10 +179,11 @@ def max_over_ranks(x, world):
 
 
 # ----------------------------------------------------------------- oracle sample
-def oracle_sample(n_heads, rows_per_head, seed=4242):
+def oracle_sample(n_heads, rows_per_head, seed=4242, threads=None):
     """Time the FP64 oracle on a bounded sample of the workload: n_heads heads,
     each restricted to rows_per_head query rows spread evenly over [0, N) (so the
-    causal work per row averages that of the whole head).  One head per thread.
+    causal work per row averages that of the whole head).  One head at a time per
+    thread, `threads` threads (default: one per head).
     Returns (seconds, algorithmic FLOPs of the sample, threads)."""
     from concurrent.futures import ThreadPoolExecutor
 
@@ -204,14 +205,15 @@ def oracle_sample(n_heads, rows_per_head, seed=4242):
         x = f64[i]
         oracle.attn_bwd_rowset(x["q"], x["k"], x["v"], x["do"], rows, scale, causal)
 
+    threads = threads or n_heads
     t0 = time.perf_counter()
-    with ThreadPoolExecutor(n_heads) as ex:
+    with ThreadPoolExecutor(threads) as ex:
         list(ex.map(one, range(n_heads)))
     dt = time.perf_counter() - t0
     # pages' convention: 14 d FLOPs (fwd 4 d + bwd 10 d) per unmasked (query, key) pair
     pairs = float(np.sum(rows + 1)) if causal else float(len(rows) * N)
     flops = 14.0 * d * pairs * n_heads
-    return dt, flops, n_heads
+    return dt, flops, threads
 
 
 def host_cores():
@@ -410,12 +412,13 @@ def run_ours(args):
     nominal = nominal_bf16_tflops(n_sm, sm_mhz)
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        n_heads = min(host_cores(), 16)
-        rows = 2048
-        dt, fl, thr = oracle_sample(n_heads, rows)
+        threads = min(host_cores(), 16)
+        n_heads = 2 * threads
+        rows = WORKLOAD["N"]
+        dt, fl, thr = oracle_sample(n_heads, rows, threads=threads)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": thr, "kind": "oracle",
-               "sample": f"{n_heads} heads x {rows} query rows (spread evenly over N) of the same workload, "
-                         f"full fwd+bwd work of those rows, {dt:.1f} s wall",
+               "sample": f"{n_heads} whole heads ({rows} query rows each) of the same workload, full fwd+bwd work, "
+                         f"{dt:.1f} s wall on {thr} threads",
                "seconds": dt}
 
     line = {
