@@ -48,6 +48,8 @@ if ROOT not in sys.path:
 
 METRIC = "attention fwd / bwd TFLOPS (BF16, d=128, causal) and % of GB300 BF16 peak"
 WORKLOAD = dict(B=8, H=16, N=4096, d=128, causal=True)
+DTYPE = "bf16"  # 16-bit type of q, k, v, dO (--shape may ask for fp16)
+DEFAULT_WORKLOAD = dict(WORKLOAD)
 WORKLOAD_NAME = "causal MHA BF16 fwd+bwd B=8 H=16 N=4096 d=128, scale 1/sqrt(128), q,k,v,dO ~ N(0,1)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -270,8 +272,8 @@ def run_ours(args):
     gen = torch.Generator(device=dev)
     gen.manual_seed(1234 + rank)
     shape = (B, H, N, d)
-    q, k, v, do = (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
-                   for _ in range(4))
+    tdt = torch.bfloat16 if DTYPE == "bf16" else torch.float16
+    q, k, v, do = (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(tdt) for _ in range(4))
     o = torch.empty_like(q)
     lse = torch.empty((B, H, N), device=dev, dtype=torch.float32)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -403,7 +405,11 @@ def run_ours(args):
     peak_sus = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     main_tflops = bwd_fl / main_ms / 1e9
-    traffic = committed_traffic("attn_bwd_kernel<128,bf16>")
+    tensor_mb = B * H * N * d * 2 / 1e6
+    l2_note = ("inputs larger than L2 (q, k, v, dO: {:.0f} MB each; 129 MB L2), no flush" if 4 * tensor_mb > 129
+               else "inputs fit in L2 (q, k, v, dO: {:.0f} MB each; 129 MB L2), no flush").format(tensor_mb)
+    # the committed counters belong to the default workload's backward
+    traffic = committed_traffic("attn_bwd_kernel<128,bf16>") if (WORKLOAD == DEFAULT_WORKLOAD and DTYPE == "bf16") else None
     fwd_tf = fwd_fl / fwd_med / 1e9
     bwd_tf = bwd_fl / bwd_med / 1e9
     # The tensor pipe's dense rate at the SM clock sampled during the timed region (the clock the
@@ -432,10 +438,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": DTYPE,
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "parallelism": f"replicas{world}",
-                   "l2": "inputs larger than L2 (q, k, v, dO: 134 MB each; 129 MB L2), no flush"},
+        "config": {"workload": WORKLOAD_NAME, **WORKLOAD, "parallelism": f"replicas{world}", "l2": l2_note},
         "fwd_tflops": fwd_tf,
         "bwd_tflops": bwd_tf,
         "fwd_pct_peak": 100.0 * fwd_tf / nominal,
@@ -451,7 +456,7 @@ def run_ours(args):
         "kernel_ms": {"attn_fwd": fwd_ms, "bwd_preprocess": pre_ms, "bwd_main": main_ms, "bwd_dq_convert": conv_ms,
                       "statistic": f"median over the {args.steps} timed steps (CUDA events per kernel)"},
         "roofline": {
-            "kernel": "attn_bwd_kernel<128,bf16> (backward main)",
+            "kernel": f"attn_bwd_kernel<{d},{DTYPE}> (backward main)",
             "bound": "tensor",
             "achieved": main_tflops,
             "peak": peak_burst,
@@ -744,7 +749,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="print fwd / bwd TFLOPS of every workload of the list instead of the bench line")
     ap.add_argument("--shape", default=None,
-                    help="B,H,N,d[,noncausal] instead of the default workload (smaller cases for profiling)")
+                    help="B,H,N,d[,noncausal][,fp16] instead of the default workload (smaller cases for profiling)")
     ap.add_argument("--dsa-shape", default=None,
                     help="s_q,s_kv,H,d_qk,topk[,causal]: time the sparse top-k backward on that shape")
     ap.add_argument("--decode-shape", default=None,
@@ -753,10 +758,11 @@ def main():
     if args.shape:
         parts = args.shape.split(",")
         WORKLOAD.update(B=int(parts[0]), H=int(parts[1]), N=int(parts[2]), d=int(parts[3]),
-                        causal=not (len(parts) > 4 and parts[4] == "noncausal"))
-        global WORKLOAD_NAME
-        WORKLOAD_NAME = ("{} MHA BF16 fwd+bwd B={B} H={H} N={N} d={d}, q,k,v,dO ~ N(0,1)"
-                         .format("causal" if WORKLOAD["causal"] else "non-causal", **WORKLOAD))
+                        causal="noncausal" not in parts[4:])
+        global WORKLOAD_NAME, DTYPE
+        DTYPE = "fp16" if "fp16" in parts[4:] else "bf16"
+        WORKLOAD_NAME = ("{} MHA {} fwd+bwd B={B} H={H} N={N} d={d}, q,k,v,dO ~ N(0,1)"
+                         .format("causal" if WORKLOAD["causal"] else "non-causal", DTYPE.upper(), **WORKLOAD))
     if args.warmup < 3:
         args.warmup = 3
     if args.gpus > 1 and "WORLD_SIZE" not in os.environ and not (args.sweep or args.decode_shape or args.dsa_shape):
