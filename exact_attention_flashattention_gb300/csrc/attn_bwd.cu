@@ -24,7 +24,8 @@
 //
 // CTA layout (512 threads): warps 0-7 elementwise (P, dS; warp w handles TMEM
 // lane quadrant w%4 and query columns [64 (w/4), +64)), warps 8-11 dQ drain
-// and dK/dV epilogue, warp 12 MMA issuer (owns TMEM), warp 13 TMA producer.
+// and dK/dV epilogue, warp 12 MMA issuer (owns TMEM), warp 13 TMA producer, warp 15
+// (packed sequences) the thread that takes units from the work counter.
 #include "attn_internal.h"
 #include "ptx.cuh"
 #include "seq.cuh"

@@ -16,10 +16,10 @@
 //   WG0 (warps 0-3)   softmax for Q tile 0 of the work item (row = thread)
 //   WG1 (warps 4-7)   softmax for Q tile 1
 //   WG2 (warps 8-11)  O correction (lazy rescale) and the epilogue
-//   WG3 warp 12       single-thread tcgen05.mma issuer (also owns TMEM)
+//   WG3 warp 12       tcgen05.mma issuer: the whole warp waits, one lane issues (also owns TMEM)
 //   WG3 warp 13       TMA producer, K/V ring
 //   WG3 warp 14       TMA producer, Q tiles
-//   WG3 warp 15       idle
+//   WG3 warp 15       idle (packed sequences: lane 0 takes units from the work counter)
 // TMEM (512 columns x 128 lanes): S0 [0,128) S1 [128,256) O0 [256,..) O1 [384,..).
 // Packed 16-bit P_q overwrites the first 64 columns of S_q.
 // Shared memory: Q0, Q1 (128 x d each) and a ring of K/V tiles (128 x d),
