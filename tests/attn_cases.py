@@ -6,9 +6,11 @@ CUDA side is reached only through the package binding.
 from __future__ import annotations
 
 import math
+from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
+import oracle
 import seeded_inputs as si
 
 
@@ -55,3 +57,21 @@ def o_tolerance(o_ref, dtype="bf16"):
     2 (as it does for the sigma = 2 inputs)."""
     half_ulp = 2.0 ** -8 if dtype == "bf16" else 2.0 ** -11
     return TOL_O_MAXABS + half_ulp * np.abs(o_ref)
+
+
+def whole_head_bwd(q, k, v, do, scale, causal, threads):
+    """dQ, dK, dV of every row of one head from the oracle's row-set entry point.  Rows are
+    dealt round robin to the threads (so causal rows of different cost spread evenly); each
+    thread returns its rows' dQ and their contributions to dK and dV, which are summed."""
+    N = q.shape[0]
+    chunks = [np.arange(t, N, threads, dtype=np.int64) for t in range(min(threads, N))]
+
+    def one(rows):
+        return oracle.attn_bwd_rowset(q, k, v, do, rows, scale, causal)
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(one, chunks))
+    dq = np.empty_like(q)
+    for rows, p in zip(chunks, parts):
+        dq[rows] = p[0]
+    return dq, sum(p[1] for p in parts), sum(p[2] for p in parts)

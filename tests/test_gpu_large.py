@@ -14,14 +14,14 @@ The worst error of each quantity over the checked heads is printed.
 """
 import math
 import os
-from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 import pytest
 
 import oracle
 import seeded_inputs as si
-from attn_cases import TOL_GRAD_RELFRO, TOL_L_MAXABS, o_tolerance, rel_fro, to_device, to_f64
+from attn_cases import (TOL_GRAD_RELFRO, TOL_L_MAXABS, o_tolerance, rel_fro, to_device, to_f64,
+                        whole_head_bwd)
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -60,24 +60,6 @@ def _sample_rows(N, rng):
     rows = {0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 2, N - 1, (N - 1) // 128 * 128}
     rows.update(int(x) for x in rng.integers(0, N, size=22))
     return np.array(sorted(r for r in rows if 0 <= r < N), dtype=np.int64)
-
-
-def _whole_head_bwd(q, k, v, do, scale, causal, threads):
-    """dQ, dK, dV of every row of one head from the oracle's row-set entry point.  Rows are
-    dealt round robin to the threads (so causal rows of different cost spread evenly); each
-    thread returns its rows' dQ and their contributions to dK and dV, which are summed."""
-    N = q.shape[0]
-    chunks = [np.arange(t, N, threads, dtype=np.int64) for t in range(min(threads, N))]
-
-    def one(rows):
-        return oracle.attn_bwd_rowset(q, k, v, do, rows, scale, causal)
-
-    with ThreadPoolExecutor(len(chunks)) as ex:
-        parts = list(ex.map(one, chunks))
-    dq = np.empty_like(q)
-    for rows, p in zip(chunks, parts):
-        dq[rows] = p[0]
-    return dq, sum(p[1] for p in parts), sum(p[2] for p in parts)
 
 
 def _whole_heads(BH, N):
@@ -148,7 +130,7 @@ def test_full_size_against_oracle(attn, cid, B, H, N, d, causal, dtype, sigma):
             le = float(np.max(np.abs(lg[h] - l_r)))
             assert le <= TOL_L_MAXABS, (h, "whole-head L", le)
             worst["l"] = max(worst["l"], le)
-        dq_r, dk_r, dv_r = _whole_head_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, threads)
+        dq_r, dk_r, dv_r = whole_head_bwd(x["q"], x["k"], x["v"], x["do"], scale, causal, threads)
         errs = {}
         for name, got, ref in (("dq", dqg[h], dq_r), ("dk", dkg[h], dk_r), ("dv", dvg[h], dv_r)):
             errs[name] = rel_fro(got, ref)
