@@ -63,3 +63,9 @@ def test_bench_gpus_flag_starts_the_ranks_itself():
     assert len(lines) == 1, out.stdout
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    # the reference arm's line carries the same metric, unit and workload as the main arm's
+    import bench
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOPS" and line["higher_is_better"] is True
+    assert line["config"]["workload"] == bench.WORKLOAD_NAME
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
