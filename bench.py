@@ -6,6 +6,8 @@ kernel, dQ conversion) over the causal BF16 workload B=8, H=16, N=4096, d=128,
 scale 1/sqrt(128), inputs ~ N(0, 1).  Prints ONE JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py --shape B,H,N,d[,noncausal][,fp16]   (another shape, for profiling)
+  python bench.py --sweep | --decode-shape ... | --dsa-shape ...   (the tables, one line each)
 
 value        whole-job TFLOPS of the step, FLOP convention fwd 4 B H N^2 d and
              bwd 10 B H N^2 d, each halved for causal; inputs resident in HBM.
